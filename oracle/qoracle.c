@@ -1,0 +1,301 @@
+/*
+ * qoracle.c -- plain, slow CPU oracle for block-quantized integer GEMM/GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the CPU-baseline leg of the benchmark may load this library.  The CUDA
+ * library shares no source, header, table or helper with it.
+ *
+ * What it computes (the method of the pages "I wrote a custom CUDA inference
+ * engine to run Qwen3.5-27B on a $130 mining card" -- Features: Q8_0 GEMM on
+ * int8 dot products -- and "A 35B Hybrid-Attention Mixture-of-Experts Model on
+ * a 6GB 2011 GPU" -- Methodology 1: W4A8 integer multiply-adds and a grouped
+ * 4-bit GEMM for MoE routing; Methodology 2: group-wise symmetric 4-bit
+ * weights with 8-bit activations):
+ *
+ *   * weights in groups of 32 along K with one binary16 scale per group,
+ *     Q8_0: d = max|w| / 127, q in [-127, 127];
+ *     Q4_0: d = max|w| / 7,   q in [-8, 7], two q per byte;
+ *   * activations in groups of 32 along K with one binary32 scale per group,
+ *     d = max|x| / 127, q in [-127, 127];
+ *   * y[m,n] = sum_g dw[n,g] * dx[m,g] * S[m,n,g],
+ *     S[m,n,g] = sum_{k in group g} qx[m,k] * qw[n,k]  (an exact integer).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - scale division is one IEEE binary32 division, q = round-half-even of the
+ *     binary32 quotient x / d, then clamped; d == 0 gives q = 0;
+ *   - a weight scale is rounded to binary16 (nearest-even, saturated at 65504)
+ *     first, and q is computed against the stored binary16 value;
+ *   - Q4 packing: byte j (0..15) of a group holds element j in its low nibble
+ *     and element j+16 in its high nibble, each stored as q + 8;
+ *   - y is summed in binary64 in group order and rounded once to binary32.
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off (never -ffast-math), optional
+ * -fopenmp: the only parallel loops are over independent output rows.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <math.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_GROUP 32
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---- binary16 <-> binary32 ------------------------------------------------
+ * IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Every finite binary16 value is n * 2^(E-10) for an integer n in [0, 2048)
+ * and E = max(exponent, -14); encode finds E from the magnitude, rounds
+ * v / 2^(E-10) to the nearest integer (ties to even; the division by a power
+ * of two is exact), and lays out the bits. A carry of n to 2048 moves into the
+ * exponent field by itself, and past the largest finite value it gives Inf. */
+uint16_t orc_f32_to_f16(float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    double v = fabs((double)f);
+    if (isinf(f) || v >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (v == 0.0) return sign;
+    int e2;
+    frexp(v, &e2);           /* v = m * 2^e2, m in [0.5, 1) */
+    int E = e2 - 1;          /* v in [2^E, 2^(E+1)) */
+    if (E < -14) E = -14;
+    double n = nearbyint(ldexp(v, 10 - E));   /* round-half-even */
+    long field = ((long)(E + 15) << 10) + (long)n - 1024;
+    return (uint16_t)(sign | (uint16_t)field);
+}
+
+float orc_f16_to_f32(uint16_t h) {
+    int s = (h >> 15) & 1, e = (h >> 10) & 0x1f, fr = h & 0x3ff;
+    double v;
+    if (e == 0x1f) v = fr ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)fr, -24);
+    else v = ldexp((double)(1024 + fr), e - 25);
+    return (float)(s ? -v : v);
+}
+
+/* ---- quantizers ------------------------------------------------------------ */
+
+static int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+/* q = clamp(round-half-even(x / d), lo, hi) in binary32; d == 0 gives 0. */
+static int quantize_one(float x, float d, int lo, int hi) {
+    if (d == 0.0f) return 0;
+    float v = x / d;
+    return clamp_int((int)rintf(v), lo, hi);
+}
+
+static float group_amax(const float* x) {
+    float a = 0.0f;
+    for (int i = 0; i < ORC_GROUP; ++i) {
+        float v = fabsf(x[i]);
+        if (v > a) a = v;
+    }
+    return a;
+}
+
+/* Activations: per row m, per 32-group g: d = amax / 127 (binary32), q int8. */
+void orc_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
+                         int8_t* qx, float* dx) {
+    int64_t G = K / ORC_GROUP;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float* xg = x + m * ldx + g * ORC_GROUP;
+            float d = group_amax(xg) / 127.0f;
+            dx[m * G + g] = d;
+            for (int i = 0; i < ORC_GROUP; ++i)
+                qx[m * K + g * ORC_GROUP + i] = (int8_t)quantize_one(xg[i], d, -127, 127);
+        }
+    }
+}
+
+/* binary16 scale from amax / qmax, saturated to the largest finite value. */
+static uint16_t weight_scale(float amax, float qmax) {
+    uint16_t h = orc_f32_to_f16(amax / qmax);
+    if ((h & 0x7fffu) == 0x7c00u) h = (uint16_t)((h & 0x8000u) | 0x7bffu);
+    return h;
+}
+
+/* Q8_0 weights: w [N][K] -> qw int8 [N][K], dw binary16 [N][G]. */
+void orc_quantize_w_q8_0(const float* w, int64_t N, int64_t K, int8_t* qw, uint16_t* dw) {
+    int64_t G = K / ORC_GROUP;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float* wg = w + n * K + g * ORC_GROUP;
+            uint16_t h = weight_scale(group_amax(wg), 127.0f);
+            float d = orc_f16_to_f32(h);
+            dw[n * G + g] = h;
+            for (int i = 0; i < ORC_GROUP; ++i)
+                qw[n * K + g * ORC_GROUP + i] = (int8_t)quantize_one(wg[i], d, -127, 127);
+        }
+    }
+}
+
+/* Q4_0 weights: w [N][K] -> qw4 uint8 [N][K/2] (nibble layout above), dw [N][G]. */
+void orc_quantize_w_q4_0(const float* w, int64_t N, int64_t K, uint8_t* qw4, uint16_t* dw) {
+    int64_t G = K / ORC_GROUP;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float* wg = w + n * K + g * ORC_GROUP;
+            uint16_t h = weight_scale(group_amax(wg), 7.0f);
+            float d = orc_f16_to_f32(h);
+            dw[n * G + g] = h;
+            int q[ORC_GROUP];
+            for (int i = 0; i < ORC_GROUP; ++i) q[i] = quantize_one(wg[i], d, -8, 7);
+            uint8_t* out = qw4 + n * (K / 2) + g * (ORC_GROUP / 2);
+            for (int j = 0; j < ORC_GROUP / 2; ++j)
+                out[j] = (uint8_t)((q[j] + 8) | ((q[j + 16] + 8) << 4));
+        }
+    }
+}
+
+/* Element k of a Q4 row (k counts from the start of the row). */
+static int q4_at(const uint8_t* row, int64_t k) {
+    int64_t g = k / ORC_GROUP, i = k % ORC_GROUP;
+    uint8_t b = row[g * (ORC_GROUP / 2) + (i % 16)];
+    int nib = (i < 16) ? (b & 0x0f) : (b >> 4);
+    return nib - 8;
+}
+
+/* ---- group dot products ---------------------------------------------------- */
+
+/* S[m][n][g] = sum_{k in g} qx[m,k] * qw[n,k]; wbits = 8 (int8 rows of K) or 4. */
+void orc_group_dots(const int8_t* qx, int64_t M, int64_t N, int64_t K,
+                    const void* qw, int wbits, int32_t* S) {
+    int64_t G = K / ORC_GROUP;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t g = 0; g < G; ++g) {
+                int32_t s = 0;
+                for (int i = 0; i < ORC_GROUP; ++i) {
+                    int64_t k = g * ORC_GROUP + i;
+                    int wv = (wbits == 8) ? ((const int8_t*)qw)[n * K + k]
+                                          : q4_at((const uint8_t*)qw + n * (K / 2), k);
+                    s += (int32_t)qx[m * K + k] * wv;
+                }
+                S[(m * N + n) * G + g] = s;
+            }
+}
+
+/* ---- y = sum_g dw * dx * S --------------------------------------------------- */
+
+/* One output row: y[n] for n in [0, N), from activation row (qxr, dxr) and the
+ * weight rows of one matrix. mag[n] = sum_g |dw * dx * S| (binary64), the scale
+ * of the terms that the tolerance of a reordered binary32 sum refers to. */
+static void row_product(const int8_t* qxr, const float* dxr, int64_t N, int64_t K,
+                        const void* qw, int wbits, const uint16_t* dw,
+                        float* yr, double* magr) {
+    int64_t G = K / ORC_GROUP;
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0, mag = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+            int64_t s = 0;
+            for (int i = 0; i < ORC_GROUP; ++i) {
+                int64_t k = g * ORC_GROUP + i;
+                int wv = (wbits == 8) ? ((const int8_t*)qw)[n * K + k]
+                                      : q4_at((const uint8_t*)qw + n * (K / 2), k);
+                s += (int64_t)qxr[k] * wv;
+            }
+            double t = (double)orc_f16_to_f32(dw[n * G + g]) * (double)dxr[g] * (double)s;
+            acc += t;
+            mag += fabs(t);
+        }
+        yr[n] = (float)acc;
+        if (magr) magr[n] = mag;
+    }
+}
+
+/* Dense GEMM/GEMV: y [M][ldy] (binary32), mag [M][N] (binary64, may be NULL). */
+void orc_qgemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+               const void* qw, int wbits, const uint16_t* dw,
+               float* y, int64_t ldy, double* mag) {
+    int64_t G = K / ORC_GROUP;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t m = 0; m < M; ++m)
+        row_product(qx + m * K, dx + m * G, N, K, qw, wbits, dw,
+                    y + m * ldy, mag ? mag + m * N : NULL);
+}
+
+/* Same as orc_qgemm for a listed subset of activation rows: row i of y/mag is
+ * activation row rows[i]. Used to check large problems on sampled rows. */
+void orc_qgemm_rows(const int8_t* qx, const float* dx, const int64_t* rows, int64_t R,
+                    int64_t N, int64_t K, const void* qw, int wbits, const uint16_t* dw,
+                    float* y, double* mag) {
+    int64_t G = K / ORC_GROUP;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < R; ++i)
+        row_product(qx + rows[i] * K, dx + rows[i] * G, N, K, qw, wbits, dw,
+                    y + i * N, mag ? mag + i * N : NULL);
+}
+
+/* ---- MoE routing and the grouped product ------------------------------------ *
+ * Pairs p = token * topk + slot. Routing groups the valid pairs by expert,
+ * keeping (token, slot) order inside each expert:
+ *   counts[e]   = number of pairs with expert e,
+ *   offsets[e]  = sum of counts[0..e-1]  (offsets[E] = number of valid pairs),
+ *   perm[...]   = the pair indices, expert by expert.
+ * Pairs whose expert id is outside [0, E) are not routed; the return value is
+ * how many there were. */
+int64_t orc_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                      int32_t* counts, int32_t* offsets, int32_t* perm) {
+    int64_t P = T * topk, bad = 0;
+    for (int32_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t p = 0; p < P; ++p) {
+        int32_t e = topk_ids[p];
+        if (e < 0 || e >= E) ++bad;
+        else ++counts[e];
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int64_t pos = 0;
+    for (int32_t e = 0; e < E; ++e)
+        for (int64_t p = 0; p < P; ++p)
+            if (topk_ids[p] == e) perm[pos++] = (int32_t)p;
+    return bad;
+}
+
+/* y[p] = x_row(p) * W_{e(p)}^T with Q4_0 expert weights qw4 [E][N][K/2], dw [E][N][G].
+ * x_row(p) is activation row p / topk (x_row_mode 0: one row per token) or p
+ * (mode 1: one row per pair). Rows of unrouted pairs are zero. Returns the
+ * number of unrouted pairs. */
+int64_t orc_grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t K,
+                              const int32_t* topk_ids, int64_t T, int32_t topk,
+                              int32_t x_row_mode, const uint8_t* qw4, const uint16_t* dw,
+                              int32_t E, int64_t N, float* y, double* mag) {
+    int64_t P = T * topk, G = K / ORC_GROUP, bad = 0;
+    for (int64_t p = 0; p < P; ++p) {
+        int32_t e = topk_ids[p];
+        if (e < 0 || e >= E) ++bad;
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t p = 0; p < P; ++p) {
+        int32_t e = topk_ids[p];
+        if (e < 0 || e >= E) {
+            for (int64_t n = 0; n < N; ++n) {
+                y[p * N + n] = 0.0f;
+                if (mag) mag[p * N + n] = 0.0;
+            }
+            continue;
+        }
+        int64_t r = x_row_mode ? p : p / topk;
+        row_product(qx + r * K, dx + r * G, N, K,
+                    qw4 + (int64_t)e * N * (K / 2), 4, dw + (int64_t)e * N * G,
+                    y + p * N, mag ? mag + p * N : NULL);
+    }
+    return bad;
+}
