@@ -1,0 +1,435 @@
+"""Benchmark of the block-quantized integer GEMM/GEMV library on GB300.
+
+Headline workload: decode GEMV at M = 1 over the four Q8_0 projections
+N x K = 4096x4096, 12288x4096, 4096x12288, 151936x4096 (weights ~ N(0, 0.02),
+activations ~ N(0, 1) with 1% of entries x20).  One step = quantize the four
+activation rows + four GEMVs.  value = algorithmic GB/s of the whole step:
+  bytes = sum over projections of N*K*(1 + 2/32) + M*K*(1 + 4/32) + M*N*4,
+the same accounting for every arm.  The per-step working set (787 MB of
+weights) is larger than L2, so no flush runs between steps.
+
+Extra sections measure the other rows of the hot path: the decode workload at
+M = 4, the prefill GEMM (M = 2048) in int8-equivalent TOPS, and the grouped
+W4A8 MoE GEMM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (weak scaling: the path has no
+exchange step); rank 0 prints one JSON line.  --impl reference times the CPU
+oracle on the host cores as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill int8 TOPS (% tensor peak); decode GEMV GB/s (% of HBM) on 1 GB300"
+DECODE_WORKLOAD = ("decode GEMV M=1, Q8_0 W8A8, N x K = 4096x4096, 12288x4096, 4096x12288, "
+                   "151936x4096; activation quantization + GEMV per projection")
+
+
+def decode_bytes(M, shapes):
+    return sum(N * K * (1 + 2 / 32) + M * K * (1 + 4 / 32) + M * N * 4 for N, K in shapes)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_decode(shapes, M, budget_s, steps_hint):
+    """Time the CPU oracle on a bounded sample of the decode workload.
+
+    Each sample step quantizes the activation rows and computes the first R
+    output rows of every projection (R chosen so the whole run stays within
+    budget_s).  Returns (GB/s, seconds per sample step, cores, description)."""
+    import oracle
+    from block_quantized_integer_gb300 import inputs
+    cases = []
+    for i, (N, K) in enumerate(shapes):
+        rng = inputs.rng_for(inputs.DECODE, 100 + i)
+        R = min(N, 4096)
+        w = inputs.normal(rng, (R, K), 0.02)
+        x = inputs.normal(rng, (M, K))
+        inputs.with_entry_outliers(rng, x, 0.01, 20.0)
+        qw, dw = oracle.quantize_w_q8_0(w)
+        cases.append((N, K, x, qw, dw))
+
+    def one(rows_frac):
+        nbytes = 0.0
+        t0 = time.perf_counter()
+        for N, K, x, qw, dw in cases:
+            R = max(1, int(qw.shape[0] * rows_frac))
+            qx, dx = oracle.quantize_act_q8(x)
+            oracle.qgemm(qx, dx, qw[:R], dw[:R], 8, want_mag=False)
+            nbytes += R * K * (1 + 2 / 32) + M * K * (1 + 4 / 32) + M * R * 4
+        return nbytes, time.perf_counter() - t0
+
+    nb, dt = one(1.0)
+    per_step = max(budget_s / max(steps_hint, 1), 0.02)
+    frac = min(1.0, per_step / max(dt, 1e-6))
+    return cases, one, frac, nb / dt / 1e9
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def make_decode(dev, M, seed_sub=0):
+    import torch
+    import block_quantized_integer_gb300 as qg
+    from block_quantized_integer_gb300 import inputs
+    projs = []
+    for i, (N, K) in enumerate(inputs.DECODE_SHAPES):
+        w, x = inputs.decode_case(N, K, M=M, sub=i + seed_sub)
+        wt = torch.from_numpy(w).to(dev)
+        qw, dw = qg.quantize_weight_q8_0(wt)
+        del wt
+        xt = torch.from_numpy(x).to(dev)
+        qx = torch.empty((M, K), dtype=torch.int8, device=dev)
+        dx = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        projs.append(dict(N=N, K=K, x=xt, qx=qx, dx=dx, qw=qw, dw=dw, y=y,
+                          x_host=torch.from_numpy(x).pin_memory(),
+                          y_host=torch.empty((M, N), dtype=torch.float32).pin_memory()))
+    torch.cuda.synchronize()
+    return projs
+
+
+def decode_step(projs, timer=None):
+    import block_quantized_integer_gb300 as qg
+    for j, p in enumerate(projs):
+        qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
+        if timer is not None and j == len(projs) - 1:
+            timer[0].record()
+        qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+        if timer is not None and j == len(projs) - 1:
+            timer[1].record()
+
+
+def decode_step_e2e(projs):
+    import block_quantized_integer_gb300 as qg
+    for p in projs:
+        p["x"].copy_(p["x_host"], non_blocking=True)
+        qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
+        qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+        p["y_host"].copy_(p["y"], non_blocking=True)
+
+
+def timed(fn, steps, warmup, dist=None, per_kernel=None):
+    """Run fn warmup times, then time `steps` calls with CUDA events on the
+    current stream, barrier + synchronize on both sides; max over ranks."""
+    import torch
+    for _ in range(warmup):
+        fn(None)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    timers = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)] if per_kernel else [None] * steps
+    start.record()
+    for i in range(steps):
+        fn(timers[i])
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    kms = None
+    if per_kernel:
+        kms = statistics.mean(a.elapsed_time(b) for a, b in timers)
+    return ms, kms
+
+
+def prefill_section(dev, peaks, reps=20):
+    """Prefill GEMM M=2048 (both shapes): int8-equivalent TOPS = 2MNK / t."""
+    import torch
+    import block_quantized_integer_gb300 as qg
+    from block_quantized_integer_gb300 import inputs
+    out = []
+    for i, (M, N, K) in enumerate(inputs.PREFILL_SHAPES):
+        w, x = inputs.prefill_case(M, N, K, sub=i)
+        qw, dw = qg.quantize_weight_q8_0(torch.from_numpy(w).to(dev))
+        qx, dx = qg.quantize_act_q8(torch.from_numpy(x).to(dev))
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            qg.qgemm_q8_0(qx, dx, qw, dw, y=y)
+        ts = []
+        for _ in range(reps):
+            scrub.fill_(1.0)                       # flush L2 (256 MB > 129 MB)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            qg.qgemm_q8_0(qx, dx, qw, dw, y=y)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops,
+                    "frac_of_bf16_peak": tops / peaks["bf16_tflops"]})
+        del qw, dw, qx, dx, y, scrub
+    return {"unit": "TOPS (int8-equivalent, 2MNK/t)", "shapes": out,
+            "peak_tflops": peaks["bf16_tflops"],
+            "peak_note": "bf16 dense tensor peak (" + peaks["source"] + "); the kernel issues "
+                         "integer-valued f16 or s8 MMA, no int8 tcgen05 form exists on sm_103a",
+            "l2": "flushed before every timed call"}
+
+
+def moe_section(dev, peaks, reps=20):
+    import torch
+    import block_quantized_integer_gb300 as qg
+    from block_quantized_integer_gb300 import inputs
+    d = inputs.moe_case()
+    ids = torch.from_numpy(d["topk_ids"]).to(dev)
+    res = {}
+    total_ms, total_bytes, total_ops = 0.0, 0.0, 0.0
+    for which, key, xkey, mode in (("gate_up", "w_gate_up", "x_tok", 0),
+                                   ("down", "w_down", "x_pair", 1)):
+        w = d[key]
+        E, N, K = w.shape
+        qw4, dw = qg.quantize_weight_q4_0(torch.from_numpy(w.reshape(E * N, K)).to(dev))
+        qw4, dw = qw4.view(E, N, K // 2), dw.view(E, N, K // 32)
+        qx, dx = qg.quantize_act_q8(torch.from_numpy(d[xkey]).to(dev))
+        P = ids.numel()
+        y = torch.empty((P, N), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(qg.workspace_size(qg.OP_GROUPED_MOE, 0, N, K, ids.shape[0],
+                                           ids.shape[1], E), dtype=torch.uint8, device=dev)
+        scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            qg.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw, y=y, d_err=err, workspace=ws)
+        ts = []
+        for _ in range(reps):
+            scrub.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            qg.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw, y=y, d_err=err, workspace=ws)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        used = np.unique(d["topk_ids"]).size
+        nbytes = used * N * K * (0.5 + 2 / 32) + qx.shape[0] * K * (1 + 4 / 32) + P * N * 4
+        ops = 2.0 * P * N * K
+        res[which] = {"E": E, "N": N, "K": K, "pairs": P, "ms": ms,
+                      "gbs": nbytes / (ms * 1e-3) / 1e9, "tops": ops / (ms * 1e-3) / 1e12}
+        total_ms += ms
+        total_bytes += nbytes
+        total_ops += ops
+        del qw4, dw, qx, dx, y, scrub
+    res["total"] = {"ms": total_ms, "gbs": total_bytes / (total_ms * 1e-3) / 1e9,
+                    "tops": total_ops / (total_ms * 1e-3) / 1e12,
+                    "frac_of_hbm": total_bytes / (total_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    res["workload"] = ("grouped W4A8 MoE, 128 experts, gate/up N=2048 (fused) K=2048 and "
+                       "down N=2048 K=1024, 947 tokens top-8 Zipf(1.1); routing included")
+    res["l2"] = "flushed before every timed call"
+    return res
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from block_quantized_integer_gb300 import inputs
+    shapes = inputs.DECODE_SHAPES
+    bytes_step = decode_bytes(1, shapes)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = 60.0
+        cases, one, frac, _ = oracle_decode(shapes, 1, budget, args.steps + args.warmup)
+        for _ in range(args.warmup):
+            one(frac)
+        tot_b, tot_t = 0.0, 0.0
+        for _ in range(args.steps):
+            b, t = one(frac)
+            tot_b += b
+            tot_t += t
+        import oracle
+        v = tot_b / tot_t / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+                "config": {"workload": DECODE_WORKLOAD, "parallelism": "replicas"},
+                "cpu_baseline": {"value": v, "unit": "GB/s",
+                                 "cores": min(oracle.num_threads(), 1),
+                                 "kind": "oracle",
+                                 "sample": f"first {frac:.4f} of the rows of each projection "
+                                           f"(at most 4096 rows), M=1, per step"},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import block_quantized_integer_gb300 as qg
+    peaks = load_peaks()
+
+    projs = make_decode(dev, 1)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ms, kms = timed(lambda tm: decode_step(projs, tm), args.steps, args.warmup, dist,
+                    per_kernel=True)
+    clocks = sampler.stop()
+    value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+
+    # end to end: pinned host x in, y out, every step
+    ms_e2e, _ = timed(lambda tm: decode_step_e2e(projs), max(args.steps // 4, 10), 3, dist)
+    e2e = world * bytes_step * max(args.steps // 4, 10) / (ms_e2e * 1e-3) / 1e9
+    h2d = sum(p["x_host"].numel() * 4 for p in projs)
+    d2h = sum(p["y_host"].numel() * 4 for p in projs)
+
+    N_lm, K_lm = shapes[-1]
+    lm_bytes = decode_bytes(1, [(N_lm, K_lm)])
+    achieved = lm_bytes / (kms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "M": 1, "parallelism": "replicas" if world > 1
+                   else "single GPU", "l2": "inputs larger than L2: 787 MB of weights per step, "
+                                            "no flush"},
+        "frac_of_hbm": value / world / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "gemv_kernel (151936x4096 Q8_0, M=1)",
+                     "peak_source": peaks["source"] + " STREAM-style copy"},
+        "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * len(projs) * args.steps,
+        "clocks": clocks,
+    }
+    del projs
+    torch.cuda.empty_cache()
+
+    if not args.no_extra and rank == 0:
+        projs4 = make_decode(dev, 4)
+        ms4, _ = timed(lambda tm: decode_step(projs4), max(args.steps // 2, 10), 5)
+        b4 = decode_bytes(4, shapes)
+        line["decode_m4"] = {"gbs": b4 * max(args.steps // 2, 10) / (ms4 * 1e-3) / 1e9,
+                             "ms_per_step": ms4 / max(args.steps // 2, 10)}
+        del projs4
+        torch.cuda.empty_cache()
+        line["prefill"] = prefill_section(dev, peaks)
+        torch.cuda.empty_cache()
+        line["moe"] = moe_section(dev, peaks)
+        torch.cuda.empty_cache()
+
+    if rank == 0:
+        _, one, frac, _ = oracle_decode(shapes, 1, 15.0, 1)
+        one(frac)
+        b, t = one(frac)
+        import oracle
+        # the oracle parallelises over activation rows only: M = 1 runs on one core
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s",
+                                "cores": min(oracle.num_threads(), 1), "kind": "oracle",
+                                "sample": f"first {frac:.4f} of the rows of each projection "
+                                          f"(at most 4096 rows), M=1, one step"}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

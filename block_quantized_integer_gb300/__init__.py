@@ -1,0 +1,172 @@
+"""Block-quantized integer GEMM/GEMV (Q8_0 / Q4_0 weights, int8 activations)
+for NVIDIA GB300 (sm_103a).
+
+Thin binding over the C ABI in ``include/qgemm.h`` (``libqgemm.so``): the
+functions below only check tensor dtypes/devices, allocate outputs with
+PyTorch when the caller passes none, and forward pointers, sizes and the
+current CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; nothing here falls back to the CPU.
+
+Tensor conventions (row-major, K contiguous, G = K // 32):
+  x   float32 [M, K]         qx int8 [M, K]      dx float32 [M, G]
+  qw  int8    [N, K]         qw4 uint8 [N, K/2]  dw float16 [N, G] (the binary16
+                                                    scales, passed as bit patterns)
+  y   float32 [M, N]
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+from ._native import QGError
+
+__all__ = [
+    "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
+    "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
+    "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "workspace_size",
+    "sm_count",
+]
+
+ALGO_AUTO, ALGO_GEMV, ALGO_MMA, ALGO_TCGEN05 = 0, 1, 2, 3
+OP_QGEMM_Q8_0, OP_QGEMM_Q4_0, OP_GROUPED_MOE = 1, 2, 3
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need(t, dtype, name, dev=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def sm_count() -> int:
+    return int(_native.load().qg_device_sm_count())
+
+
+def workspace_size(op: int, M=0, N=0, K=0, T=0, topk=0, E=0) -> int:
+    return int(_native.load().qgemm_workspace_size(op, M, N, K, T, topk, E))
+
+
+def quantize_act_q8(x: torch.Tensor, qx: torch.Tensor | None = None,
+                    dx: torch.Tensor | None = None):
+    """x float32 [M, K] -> (qx int8 [M, K], dx float32 [M, K/32])."""
+    _need(x, torch.float32, "x")
+    M, K = x.shape
+    if qx is None:
+        qx = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if dx is None:
+        dx = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    _need(qx, torch.int8, "qx", x.device)
+    _need(dx, torch.float32, "dx", x.device)
+    _native.call("quantize_act_q8", _ptr(x), M, K, x.stride(0), _ptr(qx), _ptr(dx),
+                 _stream(x.device))
+    return qx, dx
+
+
+def quantize_weight_q8_0(w: torch.Tensor):
+    """w float32 [N, K] -> (qw int8 [N, K], dw float16 [N, K/32])."""
+    _need(w, torch.float32, "w")
+    N, K = w.shape
+    qw = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    dw = torch.empty((N, K // 32), dtype=torch.float16, device=w.device)
+    _native.call("quantize_weight_q8_0", _ptr(w), N, K, _ptr(qw), _ptr(dw), _stream(w.device))
+    return qw, dw
+
+
+def quantize_weight_q4_0(w: torch.Tensor):
+    """w float32 [N, K] -> (qw4 uint8 [N, K/2], dw float16 [N, K/32])."""
+    _need(w, torch.float32, "w")
+    N, K = w.shape
+    qw4 = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    dw = torch.empty((N, K // 32), dtype=torch.float16, device=w.device)
+    _native.call("quantize_weight_q4_0", _ptr(w), N, K, _ptr(qw4), _ptr(dw), _stream(w.device))
+    return qw4, dw
+
+
+def _dense(name, qx, dx, qw, dw, y, algo, workspace, wdtype, kfac):
+    _need(qx, torch.int8, "qx")
+    dev = qx.device
+    _need(dx, torch.float32, "dx", dev)
+    _need(qw, wdtype, "qw", dev)
+    _need(dw, torch.float16, "dw", dev)
+    M, K = qx.shape
+    N = qw.shape[0]
+    if qw.shape[1] * kfac != K or dw.shape != (N, K // 32) or dx.shape != (M, K // 32):
+        raise ValueError("shape mismatch between qx/dx/qw/dw")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    else:
+        if y.dtype != torch.float32 or y.device != dev or y.stride(1) != 1:
+            raise ValueError("y must be float32 on the same device with unit column stride")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _native.call(name, _ptr(qx), _ptr(dx), M, N, K, _ptr(qw), _ptr(dw), _ptr(y), y.stride(0),
+                 ws_ptr, ws_bytes, int(algo), _stream(dev))
+    return y
+
+
+def qgemm_q8_0(qx, dx, qw, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
+    """y[m,n] = sum_g dw[n,g] dx[m,g] sum_{k in g} qx[m,k] qw[n,k] (Q8_0 weights)."""
+    return _dense("qgemm_q8_0_ex", qx, dx, qw, dw, y, algo, workspace, torch.int8, 1)
+
+
+def qgemm_q4_0(qx, dx, qw4, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
+    """As qgemm_q8_0 with Q4_0 weights qw4 uint8 [N, K/2]."""
+    return _dense("qgemm_q4_0_ex", qx, dx, qw4, dw, y, algo, workspace, torch.uint8, 2)
+
+
+def moe_route(topk_ids: torch.Tensor, E: int, d_err: torch.Tensor | None = None):
+    """topk_ids int32 [T, topk] -> (counts [E], offsets [E+1], perm [T*topk], d_err [1])."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    dev = topk_ids.device
+    T, topk = topk_ids.shape
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(T * topk, 1), dtype=torch.int32, device=dev)
+    if d_err is None:
+        d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _native.call("moe_route", _ptr(topk_ids), T, topk, E, _ptr(counts), _ptr(offsets),
+                 _ptr(perm), _ptr(d_err), _stream(dev))
+    return counts, offsets, perm, d_err
+
+
+def grouped_qgemm_moe(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y=None, d_err=None,
+                      workspace=None):
+    """Per routed pair p: y[p] = x_row(p) @ W_{e(p)}^T with Q4_0 expert weights
+    qw4 [E, N, K/2], dw float16 [E, N, K/32]; y [T*topk, N] in (token, slot) order."""
+    _need(qx, torch.int8, "qx")
+    dev = qx.device
+    _need(dx, torch.float32, "dx", dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(qw4, torch.uint8, "qw4", dev)
+    _need(dw, torch.float16, "dw", dev)
+    rows_x, K = qx.shape
+    T, topk = topk_ids.shape
+    E, N = qw4.shape[0], qw4.shape[1]
+    if y is None:
+        y = torch.empty((T * topk, N), dtype=torch.float32, device=dev)
+    if d_err is None:
+        d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        nbytes = workspace_size(OP_GROUPED_MOE, 0, N, K, T, topk, E)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _native.call("grouped_qgemm_moe", _ptr(qx), _ptr(dx), rows_x, K, _ptr(topk_ids), T, topk,
+                 int(x_row_mode), _ptr(qw4), _ptr(dw), E, N, _ptr(y), _ptr(d_err),
+                 _ptr(workspace), workspace.numel(), _stream(dev))
+    return y, d_err

@@ -1,0 +1,225 @@
+// C ABI of the library: argument validation on the host, then kernel launches
+// on the caller's stream.  See include/qgemm.h for the contract of each entry.
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/qgemm.h"
+#include "kernels.h"
+
+namespace qg {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+cudaError_t ensure_smem_attr(const void* func, int bytes, int slot) {
+    static int done[64][16] = {{0}};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || slot < 0 || slot >= 16) return cudaErrorInvalidValue;
+    if (done[dev][slot] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev][slot] = bytes;
+    return e;
+}
+
+}  // namespace qg
+
+namespace {
+
+constexpr int64_t kGroup = 32;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+qg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// MoE workspace: counts [E], offsets [E+1], tile_offsets [E+1], perm [P], int32.
+struct MoeWs {
+    size_t counts, offsets, tiles, perm, total;
+};
+MoeWs moe_ws(int64_t P, int32_t E) {
+    MoeWs w{};
+    size_t o = 0;
+    w.counts = o;  o = align_up(o + 4 * (size_t)E, 16);
+    w.offsets = o; o = align_up(o + 4 * (size_t)(E + 1), 16);
+    w.tiles = o;   o = align_up(o + 4 * (size_t)(E + 1), 16);
+    w.perm = o;    o = align_up(o + 4 * (size_t)P, 16);
+    w.total = o;
+    return w;
+}
+
+qg_status check_dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                      const void* qw, const uint16_t* dw, float* y, int64_t ldy) {
+    if (M < 0 || N <= 0 || K <= 0 || K % kGroup != 0) return QG_ERR_INVALID_ARG;
+    if (M == 0) return QG_OK;
+    if (!qx || !dx || !qw || !dw || !y) return QG_ERR_INVALID_ARG;
+    if (ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(qw) || !aligned16(y) || (ldy % 4) != 0)
+        return QG_ERR_ALIGNMENT;
+    if (!aligned16(dx) && ((uintptr_t)dx & 3u)) return QG_ERR_ALIGNMENT;
+    if ((uintptr_t)dw & 1u) return QG_ERR_ALIGNMENT;
+    return QG_OK;
+}
+
+qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
+                void* ws, size_t ws_bytes, int algo, cudaStream_t s) {
+    (void)ws; (void)ws_bytes;
+    qg_status st = check_dense(qx, dx, M, N, K, qw, dw, y, ldy);
+    if (st != QG_OK || M == 0) return st;
+    if (algo == QG_ALGO_AUTO) algo = (M <= 8) ? QG_ALGO_GEMV : QG_ALGO_MMA;
+    switch (algo) {
+        case QG_ALGO_GEMV:
+            if (M > 8) return QG_ERR_UNSUPPORTED;
+            return from_cuda(qg::launch_gemv(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
+        case QG_ALGO_MMA:
+            return from_cuda(qg::launch_mma_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
+        case QG_ALGO_TCGEN05:
+            return QG_ERR_UNSUPPORTED;
+        default:
+            return QG_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qg_status_string(qg_status s) {
+    switch (s) {
+        case QG_OK: return "QG_OK";
+        case QG_ERR_INVALID_ARG: return "QG_ERR_INVALID_ARG";
+        case QG_ERR_ALIGNMENT: return "QG_ERR_ALIGNMENT";
+        case QG_ERR_WORKSPACE: return "QG_ERR_WORKSPACE";
+        case QG_ERR_CUDA: return "QG_ERR_CUDA";
+        case QG_ERR_UNSUPPORTED: return "QG_ERR_UNSUPPORTED";
+        default: return "QG_ERR_UNKNOWN";
+    }
+}
+
+int qg_device_sm_count(void) { return qg::sm_count(); }
+
+size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
+                            int32_t E) {
+    (void)M; (void)N; (void)K;
+    if (op == QG_OP_GROUPED_MOE) {
+        if (T < 0 || topk <= 0 || E <= 0) return 0;
+        return moe_ws(T * topk, E).total;
+    }
+    return 0;
+}
+
+qg_status quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* qx,
+                          float* dx, cudaStream_t stream) {
+    if (M < 0 || K <= 0 || K % kGroup != 0 || ldx < K) return QG_ERR_INVALID_ARG;
+    if (M == 0) return QG_OK;
+    if (!x || !qx || !dx) return QG_ERR_INVALID_ARG;
+    if (!aligned16(qx) || ((uintptr_t)x & 3u) || ((uintptr_t)dx & 3u)) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_quantize_act_q8(x, M, K, ldx, qx, dx, stream));
+}
+
+static qg_status quantize_weight(const float* w, int64_t N, int64_t K, void* q, uint16_t* dw,
+                                 bool q4, cudaStream_t stream) {
+    if (N < 0 || K <= 0 || K % kGroup != 0) return QG_ERR_INVALID_ARG;
+    if (N == 0) return QG_OK;
+    if (!w || !q || !dw) return QG_ERR_INVALID_ARG;
+    if (!aligned16(q) || ((uintptr_t)w & 3u) || ((uintptr_t)dw & 1u)) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_quantize_weight(w, N, K, q, dw, q4, stream));
+}
+
+qg_status quantize_weight_q8_0(const float* w, int64_t N, int64_t K, int8_t* qw, uint16_t* dw,
+                               cudaStream_t stream) {
+    return quantize_weight(w, N, K, qw, dw, false, stream);
+}
+
+qg_status quantize_weight_q4_0(const float* w, int64_t N, int64_t K, uint8_t* qw4, uint16_t* dw,
+                               cudaStream_t stream) {
+    return quantize_weight(w, N, K, qw4, dw, true, stream);
+}
+
+qg_status qgemm_q8_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                     const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return dense(qx, dx, M, N, K, qw, false, dw, y, ldy, workspace, workspace_bytes,
+                 QG_ALGO_AUTO, stream);
+}
+
+qg_status qgemm_q4_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                     const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return dense(qx, dx, M, N, K, qw4, true, dw, y, ldy, workspace, workspace_bytes,
+                 QG_ALGO_AUTO, stream);
+}
+
+qg_status qgemm_q8_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                        const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
+                        void* workspace, size_t workspace_bytes, int algo,
+                        cudaStream_t stream) {
+    return dense(qx, dx, M, N, K, qw, false, dw, y, ldy, workspace, workspace_bytes, algo,
+                 stream);
+}
+
+qg_status qgemm_q4_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                        const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,
+                        void* workspace, size_t workspace_bytes, int algo,
+                        cudaStream_t stream) {
+    return dense(qx, dx, M, N, K, qw4, true, dw, y, ldy, workspace, workspace_bytes, algo,
+                 stream);
+}
+
+qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* d_err,
+                    cudaStream_t stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || T * (int64_t)topk >= (1ll << 31))
+        return QG_ERR_INVALID_ARG;
+    if (!topk_ids || !counts || !offsets || !perm || !d_err) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)topk_ids | (uintptr_t)counts | (uintptr_t)offsets | (uintptr_t)perm |
+         (uintptr_t)d_err) & 3u)
+        return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, nullptr,
+                                          1, nullptr, 0, d_err, stream));
+}
+
+qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, int64_t K,
+                            const int32_t* topk_ids, int64_t T, int32_t topk,
+                            int32_t x_row_mode, const uint8_t* qw4, const uint16_t* dw,
+                            int32_t E, int64_t N, float* y, int32_t* d_err, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || N <= 0 || K <= 0 || K % kGroup != 0 ||
+        (x_row_mode != 0 && x_row_mode != 1) || T * (int64_t)topk >= (1ll << 31))
+        return QG_ERR_INVALID_ARG;
+    const int64_t P = T * topk;
+    if (rows_x < (x_row_mode ? P : T)) return QG_ERR_INVALID_ARG;
+    if (T == 0) return QG_OK;
+    if (!qx || !dx || !topk_ids || !qw4 || !dw || !y || !d_err) return QG_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(qw4) || !aligned16(y) || (N % 4) != 0 ||
+        ((uintptr_t)dx & 3u) || ((uintptr_t)topk_ids & 3u) || ((uintptr_t)d_err & 3u) ||
+        ((uintptr_t)dw & 1u))
+        return QG_ERR_ALIGNMENT;
+    const MoeWs w = moe_ws(P, E);
+    if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return QG_ERR_WORKSPACE;
+    uint8_t* ws = (uint8_t*)workspace;
+    int32_t* counts = (int32_t*)(ws + w.counts);
+    int32_t* offsets = (int32_t*)(ws + w.offsets);
+    int32_t* tiles = (int32_t*)(ws + w.tiles);
+    int32_t* perm = (int32_t*)(ws + w.perm);
+    cudaError_t e = qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, tiles,
+                                         qg::mma_tile_m(), y, N, d_err, stream);
+    if (e != cudaSuccess) return QG_ERR_CUDA;
+    qg::GatherArgs ga{perm, offsets, tiles, E, topk, x_row_mode};
+    return from_cuda(qg::launch_mma_grouped(qx, dx, P, N, K, qw4, dw, y, ga, stream));
+}
+
+}  // extern "C"

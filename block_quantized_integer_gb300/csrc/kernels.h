@@ -1,0 +1,48 @@
+// Internal launchers of the CUDA library (not part of the C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qg {
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem_attr(const void* func, int bytes, int slot);
+
+struct GatherArgs {
+    const int32_t* perm;          // routed pair indices grouped by expert
+    const int32_t* offsets;       // [E+1] first position of each expert in perm
+    const int32_t* tile_offsets;  // [E+1] first m-tile of each expert
+    int32_t E;
+    int32_t topk;
+    int32_t x_row_mode;
+};
+
+cudaError_t launch_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
+                                   int8_t* qx, float* dx, cudaStream_t s);
+cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* qw,
+                                   uint16_t* dw, bool q4, cudaStream_t s);
+
+int gemv_split(int64_t N, int64_t K, bool q4, int sm);
+cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                        const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
+                        cudaStream_t s);
+
+int mma_tile_m();
+cudaError_t launch_mma_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
+                            cudaStream_t s);
+cudaError_t launch_mma_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N,
+                               int64_t K, const uint8_t* qw4, const uint16_t* dw, float* y,
+                               const GatherArgs& ga, cudaStream_t s);
+
+// Routing: counts/offsets/perm (+ m-tile offsets for tile height bm when
+// tile_offsets != nullptr; + zeroing of unrouted rows of y when y != nullptr).
+cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                             int32_t* counts, int32_t* offsets, int32_t* perm,
+                             int32_t* tile_offsets, int bm, float* y, int64_t N,
+                             int32_t* d_err, cudaStream_t s);
+
+}  // namespace qg

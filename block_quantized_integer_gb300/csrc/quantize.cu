@@ -1,0 +1,161 @@
+// Group quantizers: activations (int8, binary32 scale) and weights (Q8_0 /
+// Q4_0, binary16 scale), 32 elements per group along K.
+//
+// Rule (Q8 block format of "I wrote a custom CUDA inference engine to run
+// Qwen3.5-27B on a $130 mining card", Features; 8-bit activations and
+// group-wise symmetric 4-bit weights of "A 35B Hybrid-Attention
+// Mixture-of-Experts Model on a 6GB 2011 GPU", Methodology 2):
+//   d = max|v| / qmax by one IEEE binary32 division (__fdiv_rn),
+//   weights: d rounded to binary16 (nearest-even, saturated to 65504) first,
+//   q = clamp(round_half_even(v / d), lo, hi) with a binary32 quotient,
+//   d == 0 gives q = 0.
+// Built without --use_fast_math and without flush-to-zero, so subnormal
+// scales divide exactly as IEEE says.
+//
+// Layout of the work: 8 threads per group, 4 consecutive elements per thread
+// (one 16-byte load), a warp covers 4 groups = 512 contiguous bytes of input.
+// HBM-bound: 4 bytes read and 1.125 (activations) / 1.0625 (Q8) / 0.5625 (Q4)
+// bytes written per element.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qg {
+
+namespace {
+
+__device__ __forceinline__ float amax8(float a) {
+    // max over the 8 lanes of one group (lanes 8j .. 8j+7)
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    return a;
+}
+
+__device__ __forceinline__ int quant1(float v, float d, int lo, int hi) {
+    if (d == 0.0f) return 0;
+    int q = __float2int_rn(__fdiv_rn(v, d));
+    return min(max(q, lo), hi);
+}
+
+__device__ __forceinline__ float4 load4(const float* p, bool vec_ok) {
+    if (vec_ok) return *reinterpret_cast<const float4*>(p);
+    return make_float4(p[0], p[1], p[2], p[3]);
+}
+
+__device__ __forceinline__ uint32_t pack_s8(int a, int b, int c, int d) {
+    return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) |
+           ((uint32_t)(c & 0xff) << 16) | ((uint32_t)(d & 0xff) << 24);
+}
+
+// binary16 scale from max|v| / qmax, saturated at the largest finite value.
+__device__ __forceinline__ uint16_t scale16(float amax, float qmax) {
+    __half h = __float2half_rn(__fdiv_rn(amax, qmax));
+    uint16_t b = __half_as_ushort(h);
+    if ((b & 0x7fffu) == 0x7c00u) b = (uint16_t)((b & 0x8000u) | 0x7bffu);
+    return b;
+}
+
+__global__ void __launch_bounds__(256)
+quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                       int8_t* __restrict__ qx, float* __restrict__ dx, bool vec_ok) {
+    const int64_t G = K / kGroup;
+    const int64_t total = M * G;
+    const int sub = threadIdx.x & 7;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 3);
+    // Every lane of a warp runs the same number of iterations (the shuffles
+    // need the full warp), so the loop bound is rounded up to whole warps.
+    const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
+    const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
+    for (int64_t base = warp_first; base < total; base += stride) {
+        const int64_t grp = base + ((threadIdx.x & 31) >> 3);
+        const bool active = grp < total;
+        const int64_t m = active ? grp / G : 0, g = active ? grp % G : 0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active) v = load4(x + m * ldx + g * kGroup + sub * 4, vec_ok);
+        float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        a = amax8(a);
+        const float d = __fdiv_rn(a, 127.0f);
+        if (active) {
+            uint32_t packed = pack_s8(quant1(v.x, d, -127, 127), quant1(v.y, d, -127, 127),
+                                      quant1(v.z, d, -127, 127), quant1(v.w, d, -127, 127));
+            *reinterpret_cast<uint32_t*>(qx + m * K + g * kGroup + sub * 4) = packed;
+            if (sub == 0) dx[m * G + g] = d;
+        }
+    }
+}
+
+template <bool kQ4>
+__global__ void __launch_bounds__(256)
+quantize_weight_kernel(const float* __restrict__ w, int64_t N, int64_t K,
+                       uint8_t* __restrict__ qw, uint16_t* __restrict__ dw, bool vec_ok) {
+    const int64_t G = K / kGroup;
+    const int64_t total = N * G;
+    const int sub = threadIdx.x & 7;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 3);
+    const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
+    const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
+    const float qmax = kQ4 ? 7.0f : 127.0f;
+    const int lo = kQ4 ? -8 : -127, hi = kQ4 ? 7 : 127;
+    for (int64_t base = warp_first; base < total; base += stride) {
+        const int64_t grp = base + ((threadIdx.x & 31) >> 3);
+        const bool active = grp < total;
+        const int64_t n = active ? grp / G : 0, g = active ? grp % G : 0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active) v = load4(w + n * K + g * kGroup + sub * 4, vec_ok);
+        float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        a = amax8(a);
+        const uint16_t h = scale16(a, qmax);
+        const float d = half_bits_to_float(h);
+        int q0 = quant1(v.x, d, lo, hi), q1 = quant1(v.y, d, lo, hi);
+        int q2 = quant1(v.z, d, lo, hi), q3 = quant1(v.w, d, lo, hi);
+        if (!kQ4) {
+            if (active) {
+                *reinterpret_cast<uint32_t*>(qw + n * K + g * kGroup + sub * 4) =
+                    pack_s8(q0, q1, q2, q3);
+                if (sub == 0) dw[n * G + g] = h;
+            }
+        } else {
+            // Thread sub (0..3) holds elements 4sub..4sub+3 (low nibbles of
+            // bytes 4sub..4sub+3); thread sub+4 holds elements 16+4sub.. (the
+            // high nibbles of the same bytes).
+            uint32_t lo_n = (uint32_t)(q0 + 8) | ((uint32_t)(q1 + 8) << 8) |
+                            ((uint32_t)(q2 + 8) << 16) | ((uint32_t)(q3 + 8) << 24);
+            uint32_t hi_n = __shfl_down_sync(0xffffffffu, lo_n, 4);
+            if (active && sub < 4) {
+                *reinterpret_cast<uint32_t*>(qw + n * (K / 2) + g * (kGroup / 2) + sub * 4) =
+                    lo_n | (hi_n << 4);
+                if (sub == 0) dw[n * G + g] = h;
+            }
+        }
+    }
+}
+
+int grid_for(int64_t groups, int sm_count) {
+    int64_t need = (groups + 31) / 32;          // 32 groups per 256-thread block
+    int64_t cap = (int64_t)sm_count * 8 * 4;    // a few waves of resident blocks
+    if (need > cap) need = cap;
+    return (int)(need < 1 ? 1 : need);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
+                                   int8_t* qx, float* dx, cudaStream_t s) {
+    const bool vec_ok = ((uintptr_t)x % 16 == 0) && (ldx % 4 == 0);
+    quantize_act_q8_kernel<<<grid_for(M * (K / kGroup), sm_count()), 256, 0, s>>>(
+        x, M, K, ldx, qx, dx, vec_ok);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* qw,
+                                   uint16_t* dw, bool q4, cudaStream_t s) {
+    const bool vec_ok = ((uintptr_t)w % 16 == 0);
+    const int grid = grid_for(N * (K / kGroup), sm_count());
+    if (q4)
+        quantize_weight_kernel<true><<<grid, 256, 0, s>>>(w, N, K, (uint8_t*)qw, dw, vec_ok);
+    else
+        quantize_weight_kernel<false><<<grid, 256, 0, s>>>(w, N, K, (uint8_t*)qw, dw, vec_ok);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -1,0 +1,161 @@
+/*
+ * qgemm.h -- C ABI of the block-quantized integer GEMM/GEMV library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("I wrote a custom CUDA inference engine to run Qwen3.5-27B on
+ * a $130 mining card", Features: a Q8_0 GEMM on int8 dot products for prefill;
+ * "A 35B Hybrid-Attention Mixture-of-Experts Model on a 6GB 2011 GPU",
+ * Methodology 1: a W4A8 integer decode kernel and a grouped 4-bit GEMM for MoE
+ * routing, Methodology 2: group-wise symmetric 4-bit weights with 8-bit
+ * activations):
+ *
+ *   y[m,n] = sum_g dw[n,g] * dx[m,g] * S[m,n,g],
+ *   S[m,n,g] = sum_{k = 32g .. 32g+31} qx[m,k] * qw[n,k]     (exact integer)
+ *
+ * Data layout (all row-major, K contiguous, G = K / 32):
+ *   x    float32 [M][ldx]        activations before quantization
+ *   qx   int8    [M][K]          quantized activations, q in [-127, 127]
+ *   dx   float32 [M][G]          activation scales, d = max|x| / 127
+ *   qw   int8    [N][K]          Q8_0 weights, q in [-127, 127]
+ *   qw4  uint8   [N][K/2]        Q4_0 weights: in each 16-byte group, byte j
+ *                                holds element j (low nibble) and element
+ *                                j+16 (high nibble), each stored as q + 8
+ *   dw   uint16  [N][G]          weight scales, IEEE binary16 bit patterns
+ *   y    float32 [M][ldy]        output
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer.  The library allocates nothing, frees nothing and never
+ *     synchronizes: work is enqueued on `stream` and runs asynchronously.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     failed check returns a status and enqueues nothing.  Checks: non-null
+ *     pointers, K > 0 and K % 32 == 0, N > 0, M >= 0 (M == 0 is a no-op that
+ *     returns QG_OK), 16-byte aligned qx/qw/qw4/x/y base pointers, ld >= row
+ *     length, ldx and ldy multiples of 4.
+ *   - QG_ERR_CUDA is returned when a launch fails (cudaGetLastError after the
+ *     launch); errors of the kernels themselves surface on the stream.
+ *   - Inputs are assumed finite.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,  /* null pointer, bad size, K % 32 != 0, ld too small */
+    QG_ERR_ALIGNMENT = 2,    /* a base pointer or leading dimension is misaligned */
+    QG_ERR_WORKSPACE = 3,    /* workspace missing or smaller than qgemm_workspace_size() */
+    QG_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed */
+    QG_ERR_UNSUPPORTED = 5   /* valid request this build does not handle */
+} qg_status;
+
+/* Kernel choice for the *_ex entry points. QG_ALGO_AUTO picks by shape. */
+typedef enum {
+    QG_ALGO_AUTO = 0,
+    QG_ALGO_GEMV = 1,     /* split-K GEMV on dp4a, M <= 8 (decode) */
+    QG_ALGO_MMA = 2,      /* warp-level mma.sync int8 tile GEMM, any M */
+    QG_ALGO_TCGEN05 = 3   /* tcgen05 tensor-memory GEMM, prefill (large M) */
+} qg_algo;
+
+/* Workspace sizing: op is one of the QG_OP_* values. */
+enum { QG_OP_QGEMM_Q8_0 = 1, QG_OP_QGEMM_Q4_0 = 2, QG_OP_GROUPED_MOE = 3 };
+
+/* Human-readable name of a status. Never NULL. */
+const char* qg_status_string(qg_status s);
+
+/* Bytes of device workspace the given call needs (0 if none).  For the dense
+ * GEMMs pass M, N, K (T, topk, E ignored); for the MoE GEMM pass K and N and
+ * the routing sizes T, topk, E (M ignored). */
+size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,
+                            int64_t T, int32_t topk, int32_t E);
+
+/* Activation quantization, per row m and 32-group g (Methodology 2 of the MoE
+ * page: 8-bit activations; Q8 block rule):
+ *   d = max_k |x[m,k]| / 127  (one IEEE binary32 division, nearest-even),
+ *   q = clamp(round_half_even(x / d), -127, 127)  (binary32 quotient),
+ *   d == 0 gives q = 0.
+ * x [M][ldx] float32 (ldx >= K, ldx % 4 == 0), qx [M][K] int8, dx [M][G] float32.
+ * Bit-exact: the same bits on every run and every launch shape. */
+qg_status quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
+                          int8_t* qx, float* dx, cudaStream_t stream);
+
+/* Q8_0 weight quantization (Features of the mining-card page: Q8_0 GEMM):
+ *   d16 = binary16(max|w| / 127) (nearest-even, saturated to 65504),
+ *   q = clamp(round_half_even(w / float(d16)), -127, 127), d16 == 0 gives q = 0.
+ * w [N][K] float32 -> qw [N][K] int8, dw [N][G] binary16 bits. */
+qg_status quantize_weight_q8_0(const float* w, int64_t N, int64_t K,
+                               int8_t* qw, uint16_t* dw, cudaStream_t stream);
+
+/* Q4_0 weight quantization (Methodology 2 of the MoE page: group-wise
+ * symmetric 4-bit):  d16 = binary16(max|w| / 7), q = clamp(rhe(w / d16), -8, 7),
+ * packed as described for qw4 above.  w [N][K] -> qw4 [N][K/2], dw [N][G]. */
+qg_status quantize_weight_q4_0(const float* w, int64_t N, int64_t K,
+                               uint8_t* qw4, uint16_t* dw, cudaStream_t stream);
+
+/* Dense Q8_0 x Q8 product (prefill GEMM for large M, decode GEMV for M <= 8):
+ * y = sum_g dw * dx * S as above, every S formed exactly before it is scaled,
+ * the sum over groups in binary32 (order depends on the kernel; fixed for a
+ * given shape and algo, so results are run-to-run deterministic).
+ * workspace: pass NULL/0 when qgemm_workspace_size() returns 0. */
+qg_status qgemm_q8_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                     const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Dense Q4_0 x Q8 product: as qgemm_q8_0 with 4-bit weights qw4 [N][K/2]. */
+qg_status qgemm_q4_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                     const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* As qgemm_q8_0 / qgemm_q4_0 with an explicit kernel choice (tests and
+ * benchmarks). Returns QG_ERR_UNSUPPORTED when the kernel cannot take the
+ * shape (QG_ALGO_GEMV with M > 8). */
+qg_status qgemm_q8_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                        const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
+                        void* workspace, size_t workspace_bytes, int algo,
+                        cudaStream_t stream);
+qg_status qgemm_q4_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                        const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,
+                        void* workspace, size_t workspace_bytes, int algo,
+                        cudaStream_t stream);
+
+/* MoE routing preparation (Methodology 1 of the MoE page: grouped GEMM for
+ * MoE routing).  Pairs p = token * topk + slot, topk_ids [T][topk] int32.
+ *   counts [E]    pairs routed to each expert,
+ *   offsets [E+1] exclusive prefix sum of counts (offsets[E] = routed pairs),
+ *   perm [T*topk] pair indices grouped by expert, (token, slot) order inside
+ *                 an expert; entries past offsets[E] are left unspecified.
+ * Ids outside [0, E) are not routed: *d_err (device int32) is incremented once
+ * per such pair and nothing traps.  Deterministic.  E <= 1024, T*topk < 2^31. */
+qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* d_err,
+                    cudaStream_t stream);
+
+/* Grouped W4A8 MoE GEMM: for every routed pair p with expert e = topk_ids[p],
+ *   y[p][:] = x_row(p) * W_e^T,   W_e = Q4_0 weights qw4[e] [N][K/2], dw[e] [N][G],
+ * x_row(p) = activation row p / topk (x_row_mode 0, one row per token, rows_x
+ * >= T) or row p (x_row_mode 1, one row per pair, rows_x >= T*topk).
+ * y [T*topk][N] float32 in (token, slot) order; rows of unrouted pairs (id
+ * outside [0, E)) are set to zero and counted in *d_err.  d_err is a device
+ * int32 the caller zeroes.  Needs qgemm_workspace_size(QG_OP_GROUPED_MOE, ...)
+ * bytes of workspace (16-byte aligned). */
+qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, int64_t K,
+                            const int32_t* topk_ids, int64_t T, int32_t topk,
+                            int32_t x_row_mode, const uint8_t* qw4, const uint16_t* dw,
+                            int32_t E, int64_t N, float* y, int32_t* d_err,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int qg_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

@@ -1,0 +1,94 @@
+"""The C ABI library builds for sm_103a, loads, exports every entry point that
+include/qgemm.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_quantized_integer_gb300 import _native
+    return _native.load()
+
+
+def test_header_parses():
+    names = _declared()
+    for must in ("quantize_act_q8", "qgemm_q8_0", "qgemm_q4_0", "grouped_qgemm_moe",
+                 "moe_route", "qgemm_workspace_size", "qg_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from block_quantized_integer_gb300 import _native
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["QG_OK", "QG_ERR_INVALID_ARG", "QG_ERR_ALIGNMENT",
+                                 "QG_ERR_WORKSPACE", "QG_ERR_CUDA", "QG_ERR_UNSUPPORTED"]):
+        assert lib.qg_status_string(code).decode() == name
+
+
+A = ctypes.c_void_p(0x10000)       # 16-byte aligned fake device addresses: never dereferenced
+B = ctypes.c_void_p(0x20000)
+C = ctypes.c_void_p(0x30000)
+D = ctypes.c_void_p(0x40000)
+Y = ctypes.c_void_p(0x50000)
+NUL = ctypes.c_void_p(0)
+S = ctypes.c_void_p(0)
+
+
+def test_dense_validation(lib):
+    f = lib.qgemm_q8_0
+    assert f(A, B, 4, 256, 500, C, D, Y, 256, NUL, 0, S) == 1        # K % 32
+    assert f(A, B, 4, 0, 512, C, D, Y, 256, NUL, 0, S) == 1          # N == 0
+    assert f(A, B, -1, 256, 512, C, D, Y, 256, NUL, 0, S) == 1       # M < 0
+    assert f(A, B, 4, 256, 512, C, D, Y, 255, NUL, 0, S) == 1        # ldy < N
+    assert f(NUL, B, 4, 256, 512, C, D, Y, 256, NUL, 0, S) == 1      # null qx
+    assert f(ctypes.c_void_p(0x10008), B, 4, 256, 512, C, D, Y, 256, NUL, 0, S) == 2
+    assert f(A, B, 4, 256, 512, C, D, ctypes.c_void_p(0x50004), 256, NUL, 0, S) == 2
+    assert f(A, B, 4, 256, 512, C, D, Y, 258, NUL, 0, S) == 2        # ldy % 4
+    assert f(A, B, 0, 256, 512, C, D, Y, 256, NUL, 0, S) == 0        # M == 0: no-op
+    assert lib.qgemm_q8_0_ex(A, B, 9, 256, 512, C, D, Y, 256, NUL, 0, 1, S) == 5  # GEMV M>8
+    assert lib.qgemm_q8_0_ex(A, B, 9, 256, 512, C, D, Y, 256, NUL, 0, 77, S) == 1
+
+
+def test_quantize_validation(lib):
+    assert lib.quantize_act_q8(A, 4, 48, 48, B, C, S) == 1            # K % 32
+    assert lib.quantize_act_q8(A, 4, 64, 32, B, C, S) == 1            # ldx < K
+    assert lib.quantize_act_q8(A, 0, 64, 64, B, C, S) == 0
+    assert lib.quantize_act_q8(A, 4, 64, 64, ctypes.c_void_p(0x20001), C, S) == 2
+    assert lib.quantize_weight_q8_0(A, 4, 40, B, C, S) == 1
+    assert lib.quantize_weight_q4_0(NUL, 4, 64, B, C, S) == 1
+
+
+def test_moe_validation_and_workspace(lib):
+    ws = lib.qgemm_workspace_size(3, 0, 2048, 2048, 947, 8, 128)
+    # counts E, offsets E+1, tile offsets E+1, perm T*topk (int32, 16-byte padded)
+    assert ws >= 4 * (128 + 129 + 129 + 947 * 8)
+    assert ws % 16 == 0
+    assert lib.qgemm_workspace_size(1, 4, 256, 512, 0, 0, 0) == 0
+    g = lib.grouped_qgemm_moe
+    E = ctypes.c_void_p(0x60000)
+    W = ctypes.c_void_p(0x70000)
+    assert g(A, B, 947, 2048, C, 947, 8, 0, D, E, 128, 2048, Y, C, W, ws - 16, S) == 3
+    assert g(A, B, 947, 2048, C, 947, 8, 0, D, E, 128, 2048, Y, C, NUL, ws, S) == 3
+    assert g(A, B, 946, 2048, C, 947, 8, 0, D, E, 128, 2048, Y, C, W, ws, S) == 1  # rows_x < T
+    assert g(A, B, 947, 2048, C, 947, 8, 1, D, E, 128, 2048, Y, C, W, ws, S) == 1  # mode 1 rows
+    assert g(A, B, 947, 2048, C, 947, 8, 2, D, E, 128, 2048, Y, C, W, ws, S) == 1
+    assert g(A, B, 947, 2048, C, 947, 8, 0, D, E, 2000, 2048, Y, C, W, ws, S) == 1  # E > 1024
+    assert lib.moe_route(A, 10, 2, 2000, B, C, D, Y, S) == 1

@@ -1,0 +1,341 @@
+"""GPU parity: the CUDA kernels behind the C ABI against the CPU oracle.
+
+Bar: bit-exact for the quantized codes, the scales and every group's integer
+dot product S; y within |y - y_ref| <= 1e-5 * sum_g |dw dx S_g| per element
+(binary32 output, reordered sums).  Small cases compare every output; the
+full-size workloads (in the launch configuration the benchmark uses) compare
+sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_quantized_integer_gb300 as qg
+from block_quantized_integer_gb300 import inputs
+from helpers import assert_close, dev, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+DENSE_ALGOS = [qg.ALGO_GEMV, qg.ALGO_MMA]
+
+
+def _sync():
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ quantizers
+
+@pytest.mark.parametrize("M,K,ldx", [(4, 512, 512), (1, 4096, 4096), (37, 96, 96), (3, 32, 32),
+                                     (5, 160, 200), (2, 64, 67)])
+def test_quantize_act_bit_exact(M, K, ldx):
+    rng = np.random.default_rng(M * 1000 + K)
+    xf = rng.standard_normal((M, ldx)).astype(np.float32)
+    xf[:, rng.choice(ldx, max(1, ldx // 50), replace=False)] *= 25
+    xf[0, :32] = 0.0
+    if M > 1:
+        xf[1, :32] *= np.float32(1e-39)          # subnormal inputs and scales
+    x = xf[:, :K]
+    qx_ref, dx_ref = oracle.quantize_act_q8(x)
+    xt = to_dev(xf)[:, :K]                       # row stride ldx
+    qx, dx = qg.quantize_act_q8(xt)
+    _sync()
+    assert np.array_equal(to_np(qx), qx_ref)
+    assert np.array_equal(to_np(dx).view(np.uint32), dx_ref.view(np.uint32))
+
+
+def test_quantize_act_golden_ties():
+    rows = []
+    import os
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "q8_act_ties.txt")):
+        if line.strip() and not line.startswith("#") and not line.startswith("d "):
+            rows.append(line.split())
+    x = np.array([[float(r[0]) for r in rows]], np.float32)
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    _sync()
+    assert to_np(qx)[0].tolist() == [int(r[1]) for r in rows]
+    assert to_np(dx)[0, 0] == 1.0
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,K", [(256, 512), (300, 96), (7, 32), (1024, 2048)])
+def test_quantize_weight_bit_exact(bits, N, K):
+    rng = np.random.default_rng(N + K + bits)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[0, :32] = 0.0
+    w[min(1, N - 1), 32 % K:32 % K + 32] *= np.float32(1e-4)   # subnormal binary16 scales
+    if bits == 8:
+        q_ref, d_ref = oracle.quantize_w_q8_0(w)
+        q, d = qg.quantize_weight_q8_0(to_dev(w))
+    else:
+        q_ref, d_ref = oracle.quantize_w_q4_0(w)
+        q, d = qg.quantize_weight_q4_0(to_dev(w))
+    _sync()
+    assert np.array_equal(to_np(q), q_ref)
+    assert np.array_equal(to_np(d), d_ref)
+
+
+# ------------------------------------------------------------------ group dots
+
+def _gemm(bits, algo, qx, dx, qw, dw, y=None):
+    f = qg.qgemm_q8_0 if bits == 8 else qg.qgemm_q4_0
+    return f(qx, dx, qw, dw, y=y, algo=algo)
+
+
+@pytest.mark.parametrize("algo", DENSE_ALGOS)
+@pytest.mark.parametrize("bits", [8, 4])
+def test_group_dots_exact(algo, bits):
+    """With dx = 1 and dw = 1 on group g and 0 elsewhere, y = S[:, :, g] exactly."""
+    M = 5 if algo == qg.ALGO_GEMV else 70
+    N, K = 150, 256
+    G = K // 32
+    rng = np.random.default_rng(17 + bits + algo)
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    qx[0, :32] = 127
+    if bits == 8:
+        qw = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        qw[0, :32] = 127
+        qw[1, :32] = -127
+    else:
+        qw = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    S = oracle.group_dots(qx, qw, K, bits)
+    dx = np.ones((M, G), np.float32)
+    qx_t, dx_t, qw_t = to_dev(qx), to_dev(dx), to_dev(qw)
+    for g in range(G):
+        dw = np.zeros((N, G), np.float16)
+        dw[:, g] = 1.0
+        y = _gemm(bits, algo, qx_t, dx_t, qw_t, to_dev(dw.view(np.uint16)))
+        _sync()
+        assert np.array_equal(to_np(y), S[:, :, g].astype(np.float32)), f"group {g}"
+    if bits == 8:
+        assert S[0, 0, 0] == 32 * 127 * 127 and S[0, 1, 0] == -32 * 127 * 127
+
+
+# ------------------------------------------------------------------ dense products
+
+def _case(M, N, K, bits, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[:, rng.choice(K, max(1, K // 100), replace=False)] *= 20
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qx, dx = oracle.quantize_act_q8(x)
+    qw, dw = oracle.quantize_w_q8_0(w) if bits == 8 else oracle.quantize_w_q4_0(w)
+    return qx, dx, qw, dw
+
+
+GEMV_SHAPES = [(4, 256, 512), (1, 4096, 4096), (3, 200, 96), (8, 1000, 1024), (1, 5, 32),
+               (2, 33, 12288), (7, 129, 4160)]
+MMA_SHAPES = [(4, 256, 512), (37, 200, 96), (128, 256, 512), (300, 130, 160), (9, 1, 32),
+              (513, 384, 1056)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("algo,M,N,K", [(qg.ALGO_GEMV,) + s for s in GEMV_SHAPES] +
+                         [(qg.ALGO_MMA,) + s for s in MMA_SHAPES])
+def test_qgemm_parity(algo, M, N, K, bits):
+    qx, dx, qw, dw = _case(M, N, K, bits, M * 7 + N * 3 + K + bits)
+    y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
+    y = _gemm(bits, algo, to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    _sync()
+    assert_close(to_np(y), y_ref, mag)
+
+
+@pytest.mark.parametrize("algo", DENSE_ALGOS)
+def test_qgemm_ldy_and_determinism(algo):
+    M, N, K = (4, 300, 640) if algo == qg.ALGO_GEMV else (40, 300, 640)
+    qx, dx, qw, dw = _case(M, N, K, 8, 99)
+    y_ref, mag = oracle.qgemm(qx, dx, qw, dw, 8)
+    big = torch.full((M, N + 12), 7.0, dtype=torch.float32, device=dev())
+    args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    y1 = qg.qgemm_q8_0(*args, y=big[:, :N], algo=algo)
+    _sync()
+    assert_close(to_np(big[:, :N]), y_ref, mag)
+    assert torch.all(big[:, N:] == 7.0)                 # columns past N untouched
+    y2 = qg.qgemm_q8_0(*args, algo=algo)
+    _sync()
+    assert torch.equal(y1, y2)
+
+
+def test_qgemm_m_zero_is_noop():
+    qx = torch.empty((0, 64), dtype=torch.int8, device=dev())
+    dx = torch.empty((0, 2), dtype=torch.float32, device=dev())
+    qw = torch.zeros((8, 64), dtype=torch.int8, device=dev())
+    dw = torch.zeros((8, 2), dtype=torch.float16, device=dev())
+    y = qg.qgemm_q8_0(qx, dx, qw, dw)
+    assert y.shape == (0, 8)
+
+
+# ------------------------------------------------------------------ full-size decode
+
+@pytest.fixture(scope="module")
+def decode_weights():
+    """Q8_0 weights of the four decode projections, quantized by the oracle."""
+    out = {}
+    for i, (N, K) in enumerate(inputs.DECODE_SHAPES):
+        w, x = inputs.decode_case(N, K, M=4, sub=i)
+        qw, dw = oracle.quantize_w_q8_0(w)
+        out[(N, K)] = (w, x, qw, dw)
+    return out
+
+
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("shape", inputs.DECODE_SHAPES)
+def test_decode_full_shape(decode_weights, shape, M):
+    """The decode workload end to end through the ABI (GPU quantizes both
+    sides); codes/scales bit-exact on the oracle's, y within tolerance."""
+    w, x, qw_ref, dw_ref = decode_weights[shape]
+    x = x[:M]
+    wt = to_dev(w)
+    qw, dw = qg.quantize_weight_q8_0(wt)
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    y = qg.qgemm_q8_0(qx, dx, qw, dw)
+    _sync()
+    del wt
+    assert np.array_equal(to_np(qw), qw_ref) and np.array_equal(to_np(dw), dw_ref)
+    qx_ref, dx_ref = oracle.quantize_act_q8(x)
+    assert np.array_equal(to_np(qx), qx_ref) and np.array_equal(to_np(dx), dx_ref)
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref, dw_ref, 8)
+    assert_close(to_np(y), y_ref, mag)
+
+
+# ------------------------------------------------------------------ full-size prefill (sampled)
+
+@pytest.mark.parametrize("shape", inputs.PREFILL_SHAPES)
+def test_prefill_full_shape_sampled(shape):
+    M, N, K = shape
+    i = inputs.PREFILL_SHAPES.index(shape)
+    w, x = inputs.prefill_case(M, N, K, sub=i)
+    qw, dw = qg.quantize_weight_q8_0(to_dev(w))
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    y = qg.qgemm_q8_0(qx, dx, qw, dw)
+    _sync()
+    rows = np.sort(np.random.default_rng(5).choice(M, 12, replace=False))
+    rows[-1] = M - 1
+    qx_ref, dx_ref = oracle.quantize_act_q8(x[rows])
+    qw_ref, dw_ref = oracle.quantize_w_q8_0(w)
+    assert np.array_equal(to_np(qw), qw_ref) and np.array_equal(to_np(dw), dw_ref)
+    assert np.array_equal(to_np(qx)[rows], qx_ref)
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref, dw_ref, 8)
+    assert_close(to_np(y)[rows], y_ref, mag)
+
+
+# ------------------------------------------------------------------ MoE
+
+def _moe_small(E=9, T=53, topk=3, N=96, K=128, seed=3):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((E, N, K)) * 0.02).astype(np.float32)
+    qw4 = np.empty((E, N, K // 2), np.uint8)
+    dw = np.empty((E, N, K // 32), np.uint16)
+    for e in range(E):
+        qw4[e], dw[e] = oracle.quantize_w_q4_0(w[e])
+    ids = inputs.zipf_routing(rng, T, E, topk)
+    return rng, qw4, dw, ids
+
+
+@pytest.mark.parametrize("E,T,topk", [(9, 53, 3), (128, 947, 8), (1024, 300, 4), (5, 1, 1)])
+def test_moe_route_bit_exact(E, T, topk):
+    rng = np.random.default_rng(E + T)
+    ids = inputs.zipf_routing(rng, T, E, topk)
+    counts, offsets, perm, bad = oracle.moe_route(ids, E)
+    c, o, p, d_err = qg.moe_route(to_dev(ids), E)
+    _sync()
+    assert bad == 0 and int(to_np(d_err)[0]) == 0
+    assert np.array_equal(to_np(c), counts)
+    assert np.array_equal(to_np(o), offsets)
+    assert np.array_equal(to_np(p)[: offsets[E]], perm)
+
+
+def test_moe_route_invalid_ids():
+    ids = np.array([[0, 5], [7, 1], [-1, 0], [3, 3]], np.int32)
+    counts, offsets, perm, bad = oracle.moe_route(ids, 6)
+    c, o, p, d_err = qg.moe_route(to_dev(ids), 6)
+    _sync()
+    assert int(to_np(d_err)[0]) == bad == 2
+    assert np.array_equal(to_np(c), counts) and np.array_equal(to_np(o), offsets)
+    assert np.array_equal(to_np(p)[: offsets[6]], perm)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_grouped_moe_small(mode):
+    rng, qw4, dw, ids = _moe_small()
+    T, topk = ids.shape
+    rows = T if mode == 0 else T * topk
+    x = rng.standard_normal((rows, 128)).astype(np.float32)
+    qx, dx = oracle.quantize_act_q8(x)
+    y_ref, mag, bad = oracle.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw)
+    y, d_err = qg.grouped_qgemm_moe(to_dev(qx), to_dev(dx), to_dev(ids), mode, to_dev(qw4),
+                                    to_dev(dw))
+    _sync()
+    assert bad == 0 and int(to_np(d_err)[0]) == 0
+    assert_close(to_np(y), y_ref, mag)
+
+
+def test_grouped_moe_unrouted_rows_zero_and_counted():
+    rng, qw4, dw, ids = _moe_small()
+    ids = ids.copy()
+    ids[4, 1] = 9          # == E: out of range
+    ids[10, 0] = -2
+    x = rng.standard_normal((ids.shape[0], 128)).astype(np.float32)
+    qx, dx = oracle.quantize_act_q8(x)
+    y_ref, mag, bad = oracle.grouped_qgemm_moe(qx, dx, ids, 0, qw4, dw)
+    y0 = torch.full((ids.size, 96), 5.0, device=dev())
+    y, d_err = qg.grouped_qgemm_moe(to_dev(qx), to_dev(dx), to_dev(ids), 0, to_dev(qw4),
+                                    to_dev(dw), y=y0)
+    _sync()
+    assert bad == 2 and int(to_np(d_err)[0]) == 2
+    assert_close(to_np(y), y_ref, mag)
+
+
+def test_grouped_moe_single_expert_equals_dense_q4():
+    rng, qw4, dw, _ = _moe_small()
+    T = 300
+    ids = np.full((T, 1), 6, np.int32)
+    x = rng.standard_normal((T, 128)).astype(np.float32)
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    y, _ = qg.grouped_qgemm_moe(qx, dx, to_dev(ids), 0, to_dev(qw4), to_dev(dw))
+    yd = qg.qgemm_q4_0(qx, dx, to_dev(qw4[6]), to_dev(dw[6]), algo=qg.ALGO_MMA)
+    _sync()
+    assert torch.equal(y, yd)
+
+
+@pytest.fixture(scope="module")
+def moe_full():
+    return inputs.moe_case()
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_grouped_moe_full_config_sampled(moe_full, which):
+    d = moe_full
+    ids = d["topk_ids"]
+    E = ids.max() + 1
+    if which == "gate_up":
+        w, x, mode = d["w_gate_up"], d["x_tok"], 0
+    else:
+        w, x, mode = d["w_down"], d["x_pair"], 1
+    E, N, K = w.shape
+    wt = to_dev(w.reshape(E * N, K))
+    qw4, dw = qg.quantize_weight_q4_0(wt)
+    del wt
+    qw4 = qw4.view(E, N, K // 2)
+    dw = dw.view(E, N, K // 32)
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    y, d_err = qg.grouped_qgemm_moe(qx, dx, to_dev(ids), mode, qw4, dw)
+    _sync()
+    assert int(to_np(d_err)[0]) == 0
+    rng = np.random.default_rng(8)
+    P = ids.size
+    pairs = rng.choice(P, 48, replace=False)
+    flat = ids.ravel()
+    # the busiest expert's rows are included
+    busiest = np.bincount(flat, minlength=E).argmax()
+    pairs = np.concatenate([pairs, np.nonzero(flat == busiest)[0][-4:]])
+    yg = to_np(y)
+    qw4_np, dw_np = to_np(qw4), to_np(dw)
+    for e in np.unique(flat[pairs]):
+        q_ref, d_ref = oracle.quantize_w_q4_0(w[e])
+        assert np.array_equal(qw4_np[e], q_ref) and np.array_equal(dw_np[e], d_ref)
+        sel = pairs[flat[pairs] == e]
+        xr = sel // 8 if mode == 0 else sel
+        qx_ref, dx_ref = oracle.quantize_act_q8(x[xr])
+        y_ref, mag = oracle.qgemm(qx_ref, dx_ref, q_ref, d_ref, 4)
+        assert_close(yg[sel], y_ref, mag)
