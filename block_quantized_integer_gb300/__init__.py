@@ -26,7 +26,7 @@ __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "workspace_size",
-    "sm_count",
+    "sm_count", "device_error",
 ]
 
 ALGO_AUTO, ALGO_GEMV, ALGO_MMA, ALGO_TCGEN05 = 0, 1, 2, 3
@@ -41,7 +41,7 @@ def _stream(dev):
     return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
 
 
-def _need(t, dtype, name, dev=None):
+def _need(t, dtype, name, dev=None, rows_strided=False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -50,12 +50,20 @@ def _need(t, dtype, name, dev=None):
         raise ValueError(f"{name} must be a CUDA tensor")
     if dev is not None and t.device != dev:
         raise ValueError(f"{name} is on {t.device}, expected {dev}")
-    if not t.is_contiguous():
+    if rows_strided:
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be 2-D with unit column stride")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
 def sm_count() -> int:
     return int(_native.load().qg_device_sm_count())
+
+
+def device_error() -> int:
+    """Read and clear the tensor-core kernels' device error word (0 = none)."""
+    return int(_native.load().qg_device_error())
 
 
 def workspace_size(op: int, M=0, N=0, K=0, T=0, topk=0, E=0) -> int:
@@ -65,7 +73,7 @@ def workspace_size(op: int, M=0, N=0, K=0, T=0, topk=0, E=0) -> int:
 def quantize_act_q8(x: torch.Tensor, qx: torch.Tensor | None = None,
                     dx: torch.Tensor | None = None):
     """x float32 [M, K] -> (qx int8 [M, K], dx float32 [M, K/32])."""
-    _need(x, torch.float32, "x")
+    _need(x, torch.float32, "x", rows_strided=True)
     M, K = x.shape
     if qx is None:
         qx = torch.empty((M, K), dtype=torch.int8, device=x.device)

@@ -66,8 +66,7 @@ qg_status check_dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, i
     if (M == 0) return QG_OK;
     if (!qx || !dx || !qw || !dw || !y) return QG_ERR_INVALID_ARG;
     if (ldy < N) return QG_ERR_INVALID_ARG;
-    if (!aligned16(qx) || !aligned16(qw) || !aligned16(y) || (ldy % 4) != 0)
-        return QG_ERR_ALIGNMENT;
+    if (!aligned16(qx) || !aligned16(qw) || ((uintptr_t)y & 3u)) return QG_ERR_ALIGNMENT;
     if (!aligned16(dx) && ((uintptr_t)dx & 3u)) return QG_ERR_ALIGNMENT;
     if ((uintptr_t)dw & 1u) return QG_ERR_ALIGNMENT;
     return QG_OK;
@@ -87,7 +86,8 @@ qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t
         case QG_ALGO_MMA:
             return from_cuda(qg::launch_mma_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
         case QG_ALGO_TCGEN05:
-            return QG_ERR_UNSUPPORTED;
+            if (q4 || !qg::tc_gemm_supported(M, N, K, dx, dw)) return QG_ERR_UNSUPPORTED;
+            return from_cuda(qg::launch_tc_gemm(qx, dx, M, N, K, (const int8_t*)qw, dw, y, ldy, s));
         default:
             return QG_ERR_INVALID_ARG;
     }
@@ -110,6 +110,8 @@ const char* qg_status_string(qg_status s) {
 }
 
 int qg_device_sm_count(void) { return qg::sm_count(); }
+
+unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
                             int32_t E) {
@@ -204,7 +206,7 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
     if (rows_x < (x_row_mode ? P : T)) return QG_ERR_INVALID_ARG;
     if (T == 0) return QG_OK;
     if (!qx || !dx || !topk_ids || !qw4 || !dw || !y || !d_err) return QG_ERR_INVALID_ARG;
-    if (!aligned16(qx) || !aligned16(qw4) || !aligned16(y) || (N % 4) != 0 ||
+    if (!aligned16(qx) || !aligned16(qw4) || ((uintptr_t)y & 3u) ||
         ((uintptr_t)dx & 3u) || ((uintptr_t)topk_ids & 3u) || ((uintptr_t)d_err & 3u) ||
         ((uintptr_t)dw & 1u))
         return QG_ERR_ALIGNMENT;

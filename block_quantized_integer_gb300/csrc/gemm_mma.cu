@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 mma_gemm_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, int64_t M,
                 int64_t N, int64_t K, const uint8_t* __restrict__ qw,
                 const uint16_t* __restrict__ dw, float* __restrict__ y, int64_t ldy,
-                GatherArgs ga, int n_tiles) {
+                GatherArgs ga, int n_tiles, bool vec2) {
     extern __shared__ __align__(128) uint8_t smem[];
     using S = Smem<kQ4>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -286,8 +286,11 @@ mma_gemm_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, int
             for (int nt = 0; nt < 4; ++nt) {
                 const int64_t c = n0 + warp_n * 32 + nt * 8 + (lane & 3) * 2;
                 const float v0 = acc[mt][nt][2 * h], v1 = acc[mt][nt][2 * h + 1];
-                if (c + 1 < N) {
+                if (vec2 && c + 1 < N) {
                     *reinterpret_cast<float2*>(yr + c) = make_float2(v0, v1);
+                } else if (c + 1 < N) {
+                    yr[c] = v0;
+                    yr[c + 1] = v1;
                 } else if (c < N) {
                     yr[c] = v0;
                 }
@@ -303,8 +306,9 @@ cudaError_t launch(dim3 grid, const int8_t* qx, const float* dx, int64_t M, int6
     cudaError_t e = ensure_smem_attr((const void*)mma_gemm_kernel<kQ4, kGather>, smem,
                                      (kQ4 ? 1 : 0) + (kGather ? 2 : 0));
     if (e != cudaSuccess) return e;
+    const bool vec2 = ((uintptr_t)y % 8 == 0) && (ldy % 2 == 0);
     mma_gemm_kernel<kQ4, kGather><<<grid, THREADS, smem, s>>>(qx, dx, M, N, K, qw, dw, y, ldy,
-                                                               ga, n_tiles);
+                                                               ga, n_tiles, vec2);
     return cudaGetLastError();
 }
 

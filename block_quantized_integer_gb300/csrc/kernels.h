@@ -38,6 +38,12 @@ cudaError_t launch_mma_grouped(const int8_t* qx, const float* dx, int64_t P, int
                                int64_t K, const uint8_t* qw4, const uint16_t* dw, float* y,
                                const GatherArgs& ga, cudaStream_t s);
 
+bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const void* dw);
+cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
+                           const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
+                           cudaStream_t s);
+unsigned int read_and_clear_tc_error();
+
 // Routing: counts/offsets/perm (+ m-tile offsets for tile height bm when
 // tile_offsets != nullptr; + zeroing of unrouted rows of y when y != nullptr).
 cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,

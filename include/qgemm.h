@@ -30,8 +30,8 @@
  *   - Arguments are validated on the host before anything is enqueued; a
  *     failed check returns a status and enqueues nothing.  Checks: non-null
  *     pointers, K > 0 and K % 32 == 0, N > 0, M >= 0 (M == 0 is a no-op that
- *     returns QG_OK), 16-byte aligned qx/qw/qw4/x/y base pointers, ld >= row
- *     length, ldx and ldy multiples of 4.
+ *     returns QG_OK), 16-byte aligned qx/qw/qw4 base pointers, 4-byte aligned
+ *     x/dx/y, 2-byte aligned dw, ld >= row length.
  *   - QG_ERR_CUDA is returned when a launch fails (cudaGetLastError after the
  *     launch); errors of the kernels themselves surface on the stream.
  *   - Inputs are assumed finite.
@@ -81,7 +81,7 @@ size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,
  *   d = max_k |x[m,k]| / 127  (one IEEE binary32 division, nearest-even),
  *   q = clamp(round_half_even(x / d), -127, 127)  (binary32 quotient),
  *   d == 0 gives q = 0.
- * x [M][ldx] float32 (ldx >= K, ldx % 4 == 0), qx [M][K] int8, dx [M][G] float32.
+ * x [M][ldx] float32 (ldx >= K), qx [M][K] int8, dx [M][G] float32.
  * Bit-exact: the same bits on every run and every launch shape. */
 qg_status quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
                           int8_t* qx, float* dx, cudaStream_t stream);
@@ -153,6 +153,12 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
 
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int qg_device_sm_count(void);
+
+/* Device error word of the tensor-core kernels on the current device, then
+ * cleared: 0 = none, bit 0 = a pipeline wait gave up (the kernel abandoned its
+ * tile without writing it, after draining its own copies and freeing tensor
+ * memory).  Synchronizes with the device (a blocking copy). */
+unsigned int qg_device_error(void);
 
 #ifdef __cplusplus
 }

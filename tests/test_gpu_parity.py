@@ -17,7 +17,7 @@ from helpers import assert_close, dev, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
-DENSE_ALGOS = [qg.ALGO_GEMV, qg.ALGO_MMA]
+DENSE_ALGOS = [qg.ALGO_GEMV, qg.ALGO_MMA, qg.ALGO_TCGEN05]
 
 
 def _sync():
@@ -86,8 +86,10 @@ def _gemm(bits, algo, qx, dx, qw, dw, y=None):
 @pytest.mark.parametrize("bits", [8, 4])
 def test_group_dots_exact(algo, bits):
     """With dx = 1 and dw = 1 on group g and 0 elsewhere, y = S[:, :, g] exactly."""
+    if algo == qg.ALGO_TCGEN05 and bits == 4:
+        pytest.skip("the tcgen05 dense kernel takes Q8_0 weights")
     M = 5 if algo == qg.ALGO_GEMV else 70
-    N, K = 150, 256
+    N, K = (150, 256) if algo != qg.ALGO_TCGEN05 else (300, 512)
     G = K // 32
     rng = np.random.default_rng(17 + bits + algo)
     qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
@@ -109,6 +111,7 @@ def test_group_dots_exact(algo, bits):
         assert np.array_equal(to_np(y), S[:, :, g].astype(np.float32)), f"group {g}"
     if bits == 8:
         assert S[0, 0, 0] == 32 * 127 * 127 and S[0, 1, 0] == -32 * 127 * 127
+    assert qg.device_error() == 0
 
 
 # ------------------------------------------------------------------ dense products
@@ -127,22 +130,28 @@ GEMV_SHAPES = [(4, 256, 512), (1, 4096, 4096), (3, 200, 96), (8, 1000, 1024), (1
                (2, 33, 12288), (7, 129, 4160)]
 MMA_SHAPES = [(4, 256, 512), (37, 200, 96), (128, 256, 512), (300, 130, 160), (9, 1, 32),
               (513, 384, 1056)]
+TC_SHAPES = [(4, 256, 512), (128, 256, 256), (300, 130, 768), (129, 513, 1024), (9, 1, 256),
+             (256, 768, 4096), (640, 1000, 2048)]
 
 
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("algo,M,N,K", [(qg.ALGO_GEMV,) + s for s in GEMV_SHAPES] +
-                         [(qg.ALGO_MMA,) + s for s in MMA_SHAPES])
+                         [(qg.ALGO_MMA,) + s for s in MMA_SHAPES] +
+                         [(qg.ALGO_TCGEN05,) + s for s in TC_SHAPES])
 def test_qgemm_parity(algo, M, N, K, bits):
+    if algo == qg.ALGO_TCGEN05 and bits == 4:
+        pytest.skip("the tcgen05 dense kernel takes Q8_0 weights")
     qx, dx, qw, dw = _case(M, N, K, bits, M * 7 + N * 3 + K + bits)
     y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
     y = _gemm(bits, algo, to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
     _sync()
     assert_close(to_np(y), y_ref, mag)
+    assert qg.device_error() == 0
 
 
 @pytest.mark.parametrize("algo", DENSE_ALGOS)
 def test_qgemm_ldy_and_determinism(algo):
-    M, N, K = (4, 300, 640) if algo == qg.ALGO_GEMV else (40, 300, 640)
+    M, N, K = (4, 300, 640) if algo == qg.ALGO_GEMV else (40, 300, 768)
     qx, dx, qw, dw = _case(M, N, K, 8, 99)
     y_ref, mag = oracle.qgemm(qx, dx, qw, dw, 8)
     big = torch.full((M, N + 12), 7.0, dtype=torch.float32, device=dev())
@@ -200,15 +209,17 @@ def test_decode_full_shape(decode_weights, shape, M):
 
 # ------------------------------------------------------------------ full-size prefill (sampled)
 
+@pytest.mark.parametrize("algo", [qg.ALGO_AUTO, qg.ALGO_TCGEN05, qg.ALGO_MMA])
 @pytest.mark.parametrize("shape", inputs.PREFILL_SHAPES)
-def test_prefill_full_shape_sampled(shape):
+def test_prefill_full_shape_sampled(shape, algo):
     M, N, K = shape
     i = inputs.PREFILL_SHAPES.index(shape)
     w, x = inputs.prefill_case(M, N, K, sub=i)
     qw, dw = qg.quantize_weight_q8_0(to_dev(w))
     qx, dx = qg.quantize_act_q8(to_dev(x))
-    y = qg.qgemm_q8_0(qx, dx, qw, dw)
+    y = qg.qgemm_q8_0(qx, dx, qw, dw, algo=algo)
     _sync()
+    assert qg.device_error() == 0
     rows = np.sort(np.random.default_rng(5).choice(M, 12, replace=False))
     rows[-1] = M - 1
     qx_ref, dx_ref = oracle.quantize_act_q8(x[rows])
