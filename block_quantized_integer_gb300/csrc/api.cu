@@ -78,7 +78,11 @@ qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t
     (void)ws; (void)ws_bytes;
     qg_status st = check_dense(qx, dx, M, N, K, qw, dw, y, ldy);
     if (st != QG_OK || M == 0) return st;
-    if (algo == QG_ALGO_AUTO) algo = (M <= 8) ? QG_ALGO_GEMV : QG_ALGO_MMA;
+    if (algo == QG_ALGO_AUTO) {
+        if (M <= 8) algo = QG_ALGO_GEMV;
+        else if (!q4 && qg::tc_gemm_supported(M, N, K, dx, dw)) algo = QG_ALGO_TCGEN05;
+        else algo = QG_ALGO_MMA;
+    }
     switch (algo) {
         case QG_ALGO_GEMV:
             if (M > 8) return QG_ERR_UNSUPPORTED;
