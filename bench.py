@@ -313,8 +313,28 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
+    ap.add_argument("--only", choices=["prefill", "moe", "decode"], default=None,
+                    help="run one section only (for profiling); prints its JSON")
+    ap.add_argument("--reps", type=int, default=20, help="timed calls per prefill/MoE shape")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only is not None:
+        import torch
+        dev = torch.device("cuda", 0)
+        peaks = load_peaks()
+        if args.only == "prefill":
+            out = prefill_section(dev, peaks, reps=args.reps)
+        elif args.only == "moe":
+            out = moe_section(dev, peaks, reps=args.reps)
+        else:
+            projs = make_decode(dev, 1)
+            ms, kms = timed(lambda tm: decode_step(projs, tm), args.steps, args.warmup, None,
+                            per_kernel=True)
+            from block_quantized_integer_gb300 import inputs as _in
+            out = {"gbs": decode_bytes(1, _in.DECODE_SHAPES) * args.steps / (ms * 1e-3) / 1e9,
+                   "lm_head_ms": kms}
+        print(json.dumps(out), flush=True)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -410,9 +430,9 @@ def main():
                              "ms_per_step": ms4 / max(args.steps // 2, 10)}
         del projs4
         torch.cuda.empty_cache()
-        line["prefill"] = prefill_section(dev, peaks)
+        line["prefill"] = prefill_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
-        line["moe"] = moe_section(dev, peaks)
+        line["moe"] = moe_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
 
     if rank == 0:
