@@ -25,7 +25,8 @@ from ._native import QGError
 __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
-    "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "workspace_size",
+    "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
+    "workspace_size",
     "sm_count", "device_error",
 ]
 
@@ -177,4 +178,26 @@ def grouped_qgemm_moe(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y=None, d_err=
     _native.call("grouped_qgemm_moe", _ptr(qx), _ptr(dx), rows_x, K, _ptr(topk_ids), T, topk,
                  int(x_row_mode), _ptr(qw4), _ptr(dw), E, N, _ptr(y), _ptr(d_err),
                  _ptr(workspace), workspace.numel(), _stream(dev))
+    return y, d_err
+
+
+def grouped_qgemm_moe_noalloc(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y, d_err):
+    """grouped_qgemm_moe through the entry point that allocates nothing: the
+    routing scratch is a fixed array inside the library (at most 65536 routed
+    pairs and 1024 experts).  For callers that cannot allocate device memory,
+    y and d_err (zeroed by the caller) must be passed in."""
+    _need(qx, torch.int8, "qx")
+    dev = qx.device
+    _need(dx, torch.float32, "dx", dev)
+    _need(topk_ids, torch.int32, "topk_ids", dev)
+    _need(qw4, torch.uint8, "qw4", dev)
+    _need(dw, torch.float16, "dw", dev)
+    _need(y, torch.float32, "y", dev)
+    _need(d_err, torch.int32, "d_err", dev)
+    rows_x, K = qx.shape
+    T, topk = topk_ids.shape
+    E, N = qw4.shape[0], qw4.shape[1]
+    _native.call("grouped_qgemm_moe_noalloc", _ptr(qx), _ptr(dx), rows_x, K, _ptr(topk_ids), T,
+                 topk, int(x_row_mode), _ptr(qw4), _ptr(dw), E, N, _ptr(y), _ptr(d_err),
+                 _stream(dev))
     return y, d_err

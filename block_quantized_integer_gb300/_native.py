@@ -35,6 +35,8 @@ SIGNATURES = {
     "moe_route": (ctypes.c_int, [P, I64, I32, I32, P, P, P, P, P]),
     "grouped_qgemm_moe": (ctypes.c_int, [P, P, I64, I64, P, I64, I32, I32, P, P, I32, I64, P,
                                          P, P, SZ, P]),
+    "grouped_qgemm_moe_noalloc": (ctypes.c_int, [P, P, I64, I64, P, I64, I32, I32, P, P, I32,
+                                                 I64, P, P, P]),
 }
 
 

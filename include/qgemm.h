@@ -151,6 +151,28 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
                             int32_t E, int64_t N, float* y, int32_t* d_err,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* grouped_qgemm_moe for callers that cannot allocate device memory: same
+ * arguments, results and errors as grouped_qgemm_moe, minus the workspace.
+ * (No counterpart in the pages this library follows: it exists for callers
+ * such as a serving process whose device memory is reserved up front by its
+ * own pool allocator and that may not call cudaMalloc while running, or a
+ * plugin host that passes in buffers but grants no allocation rights.)
+ * The routing scratch lives in a fixed array inside the library, held on every
+ * GPU that loads it until the process exits: at most 65536 routed pairs
+ * (T * topk) and 1024 experts, about 270 KiB; larger requests return
+ * QG_ERR_UNSUPPORTED before anything is enqueued.  The call allocates and
+ * frees nothing.  Every call rewrites the scratch it reads, so nothing in it
+ * needs zeroing (d_err is still zeroed by the caller).  All calls share the one
+ * array: calls that overlap on the GPU (unordered streams) race on it.  The
+ * first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. */
+qg_status grouped_qgemm_moe_noalloc(const int8_t* qx, const float* dx, int64_t rows_x, int64_t K,
+                                    const int32_t* topk_ids, int64_t T, int32_t topk,
+                                    int32_t x_row_mode, const uint8_t* qw4, const uint16_t* dw,
+                                    int32_t E, int64_t N, float* y, int32_t* d_err,
+                                    cudaStream_t stream);
+
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int qg_device_sm_count(void);
 
