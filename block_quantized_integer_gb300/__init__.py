@@ -122,6 +122,11 @@ def _dense(name, qx, dx, qw, dw, y, algo, workspace, wdtype, kfac):
     else:
         if y.dtype != torch.float32 or y.device != dev or y.stride(1) != 1:
             raise ValueError("y must be float32 on the same device with unit column stride")
+    if workspace is None:
+        op = OP_QGEMM_Q8_0 if kfac == 1 else OP_QGEMM_Q4_0
+        nbytes = workspace_size(op, M, N, K)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()

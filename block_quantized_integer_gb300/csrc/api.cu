@@ -72,15 +72,20 @@ qg_status check_dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, i
     return QG_OK;
 }
 
+// Dense products with M > 8 run on the tcgen05 kernel when K % 256 == 0 and
+// the scale planes are 16-byte aligned (TMA boxes), else on the warp-MMA one.
+bool use_tc(int64_t M, int64_t N, int64_t K, const void* dx, const void* dw) {
+    return M > 8 && qg::tc_gemm_supported(M, N, K, dx, dw);
+}
+
 qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                 const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                 void* ws, size_t ws_bytes, int algo, cudaStream_t s) {
-    (void)ws; (void)ws_bytes;
     qg_status st = check_dense(qx, dx, M, N, K, qw, dw, y, ldy);
     if (st != QG_OK || M == 0) return st;
     if (algo == QG_ALGO_AUTO) {
         if (M <= 8) algo = QG_ALGO_GEMV;
-        else if (!q4 && qg::tc_gemm_supported(M, N, K, dx, dw)) algo = QG_ALGO_TCGEN05;
+        else if (use_tc(M, N, K, dx, dw)) algo = QG_ALGO_TCGEN05;
         else algo = QG_ALGO_MMA;
     }
     switch (algo) {
@@ -90,8 +95,10 @@ qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t
         case QG_ALGO_MMA:
             return from_cuda(qg::launch_mma_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
         case QG_ALGO_TCGEN05:
-            if (q4 || !qg::tc_gemm_supported(M, N, K, dx, dw)) return QG_ERR_UNSUPPORTED;
-            return from_cuda(qg::launch_tc_gemm(qx, dx, M, N, K, (const int8_t*)qw, dw, y, ldy, s));
+            if (!qg::tc_gemm_supported(M, N, K, dx, dw)) return QG_ERR_UNSUPPORTED;
+            if (!ws || ws_bytes < qg::tc_gemm_workspace(M, K) || !aligned16(ws))
+                return QG_ERR_WORKSPACE;
+            return from_cuda(qg::launch_tc_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, ws, s));
         default:
             return QG_ERR_INVALID_ARG;
     }
@@ -119,10 +126,15 @@ unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
                             int32_t E) {
-    (void)M; (void)N; (void)K;
+    (void)N;
     if (op == QG_OP_GROUPED_MOE) {
         if (T < 0 || topk <= 0 || E <= 0) return 0;
         return moe_ws(T * topk, E).total;
+    }
+    if (op == QG_OP_QGEMM_Q8_0 || op == QG_OP_QGEMM_Q4_0) {
+        // the tensor-core path widens the activation codes to binary16 first
+        if (M > 8 && K > 0 && K % 256 == 0) return qg::tc_gemm_workspace(M, K);
+        return 0;
     }
     return 0;
 }

@@ -4,26 +4,31 @@
 // product of one 32-group ("I wrote a custom CUDA inference engine to run
 // Qwen3.5-27B on a $130 mining card", Features: the Q8_0 GEMM tile path of the
 // prefill; "A 35B Hybrid-Attention Mixture-of-Experts Model on a 6GB 2011 GPU",
-// Methodology 4: one pass over the whole prompt keeps the GEMM M large).
+// Methodology 1: grouped 4-bit GEMM for MoE routing; Methodology 4: one pass
+// over the whole prompt keeps the GEMM M large).
 //
-// sm_103a has no integer tcgen05 MMA form, so the int8 codes are widened to
+// sm_103a has no integer tcgen05 MMA form, so the codes are widened to
 // binary16, where every value in [-127, 127] is exact, and multiplied with
 // kind::f16 into binary32 tensor memory: each product is an integer below
-// 2^14 and each group sum an integer below 2^19, exact as long as the tensor
-// core accumulates a 32-term integer sum without loss (the group-dot tests
-// check this bit for bit on extreme groups).
+// 2^14 and each group sum an integer below 2^19, which the tensor core
+// accumulates without loss (the group-dot tests check this bit for bit).
 //
-// Per CTA: a 128 x 256 output tile, K walked one 32-group at a time.
-//   warp 8      TMA producer: int8 A/B tiles, 4 groups per stage, 128-byte
-//               swizzle; dx / dw scale tiles every 8 groups.
-//   warps 10-11 converters: int8 -> binary16 into the canonical K-major
-//               no-swizzle operand layout (8x16-byte core matrices), one
-//               32-group per operand buffer, 3 buffers.
-//   warp 9      one thread issues two K=16 MMAs per group into one of two
-//               256-column TMEM accumulators (first with D overwritten).
-//   warps 0-7   epilogue: tcgen05.ld of the group's exact partial, then
-//               y += S * (dx * dw) into binary32 registers (thread = row,
-//               warpgroup = 128 columns); y is written once at the end.
+// Per CTA: a 128 x 128 output tile, K walked one 32-group at a time.
+//   pre-pass    activation codes widened to binary16 once per call (for the
+//               MoE product also gathered into expert order with their scales).
+//   warp 8      TMA producer: binary16 A tiles (2 groups per stage, 128-byte
+//               swizzle, the operand layout the MMA reads directly), int8 or
+//               packed 4-bit B tiles (4 / 8 groups per stage, 128-byte
+//               swizzle), dx / dw scale tiles every 8 groups.
+//   warps 10-11 converters: B codes -> binary16 into the canonical K-major
+//               no-swizzle layout (8 x 16-byte core matrices), one group per
+//               buffer, 4 buffers; dw -> binary32 once per 8 groups.
+//   warp 9      one thread issues two K=16 MMAs per group into one of four
+//               128-column TMEM buffers (the first MMA overwrites).
+//   warps 0-7   epilogue: one tcgen05.ld round trip fetches a group's 64
+//               partials per thread (row = TMEM lane, warpgroup = 64 columns);
+//               the buffer is released at once and y += S * (dx * dw) runs on
+//               packed f32x2 instructions into binary32 registers.
 // Every mbarrier wait is bounded; on a timeout the CTA sets a device error
 // word, drains its own TMA copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -40,56 +45,60 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256;
-constexpr int GS = 4;                   // groups per int8 TMA stage (128 bytes of K)
-constexpr int NS = 2;                   // int8 stages
-constexpr int NF = 3;                   // binary16 operand buffers (one group each)
-constexpr int SCG = 8;                  // groups per scale stage
+constexpr int BM = 128, BN = 128;
+constexpr int GA = 2;                  // groups per A stage (64 binary16 = 128-byte rows)
+constexpr int NA = 5;                  // A stages
+constexpr int NB = 4;                  // B stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
+constexpr int NF = 4;                  // binary16 B buffers (one group each)
+constexpr int NT = 4;                  // TMEM accumulator buffers (128 columns each)
+constexpr int SCG = 8;                 // groups per scale stage
+constexpr int NSC = 3;                 // scale stages
 constexpr int THREADS = 384;
-constexpr int EPI_THREADS = 256;
+constexpr int EPI_WARPS = 8;
 constexpr int CONV_WARP0 = 10, CONV_WARPS = 2, CONV_THREADS = CONV_WARPS * 32;
 
-constexpr int I8_A_BYTES = BM * GS * 32;             // 16384
-constexpr int I8_B_BYTES = BN * GS * 32;             // 32768
-constexpr int I8_STAGE = I8_A_BYTES + I8_B_BYTES;    // 49152
-constexpr int F16_A_BYTES = BM * 32 * 2;             // 8192
-constexpr int F16_B_BYTES = BN * 32 * 2;             // 16384
-constexpr int F16_STAGE = F16_A_BYTES + F16_B_BYTES; // 24576
+constexpr int A_STAGE = BM * 128;                    // 16384
+constexpr int B_STAGE = BN * 128;                    // 16384
+constexpr int F16_B = BN * 32 * 2;                   // 8192
 constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128][8] f32
-constexpr int SC_DW = BN * SCG * 2;                  // 4096: dw [256][8] f16
-constexpr int SC_DWF = SCG * BN * 4;                 // 8192: dw [8][256] f32
-constexpr int SC_STAGE = SC_DX + SC_DW + SC_DWF;     // 16384
+constexpr int SC_DW = BN * SCG * 2;                  // 2048: dw [128][8] f16
+constexpr int SC_DWF = SCG * BN * 4;                 // 4096: dw [8][128] f32
+constexpr int SC_STAGE = SC_DX + SC_DW + SC_DWF;     // 10240
 
-constexpr int OFF_I8 = 0;
-constexpr int OFF_F16 = OFF_I8 + NS * I8_STAGE;
-constexpr int OFF_SC = OFF_F16 + NF * F16_STAGE;
-constexpr int OFF_BAR = OFF_SC + 2 * SC_STAGE;
-constexpr int NUM_BARS = 2 * NS + 2 * NF + 3 * 2 + 2 * 2 + 1;
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NA * A_STAGE;
+constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
+constexpr int OFF_SC = OFF_F16 + NF * F16_B;
+constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
+constexpr int NUM_BARS = 2 * NA + 2 * NB + 2 * NF + 3 * NSC + 2 * NT + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 KiB alignment");
 
-constexpr uint32_t TMEM_COLS = 512;     // two 256-column accumulators
+constexpr uint32_t TMEM_COLS = NT * BN;               // 512
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 struct Bars {
-    uint32_t full_i8, empty_i8, full_f16, empty_f16, full_sc, ready_sc, empty_sc, tfull,
-        tempty, drain;
+    uint32_t full_a, empty_a, full_b, empty_b, full_f16, empty_f16, full_sc, ready_sc, empty_sc,
+        tfull, tempty, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
     Bars b;
-    b.full_i8 = base;
-    b.empty_i8 = b.full_i8 + NS * 8;
-    b.full_f16 = b.empty_i8 + NS * 8;
-    b.empty_f16 = b.full_f16 + NF * 8;
-    b.full_sc = b.empty_f16 + NF * 8;
-    b.ready_sc = b.full_sc + 16;
-    b.empty_sc = b.ready_sc + 16;
-    b.tfull = b.empty_sc + 16;
-    b.tempty = b.tfull + 16;
-    b.drain = b.tempty + 16;
+    b.full_a = base;
+    b.empty_a = b.full_a + 8 * NA;
+    b.full_b = b.empty_a + 8 * NA;
+    b.empty_b = b.full_b + 8 * NB;
+    b.full_f16 = b.empty_b + 8 * NB;
+    b.empty_f16 = b.full_f16 + 8 * NF;
+    b.full_sc = b.empty_f16 + 8 * NF;
+    b.ready_sc = b.full_sc + 8 * NSC;
+    b.empty_sc = b.ready_sc + 8 * NSC;
+    b.tfull = b.empty_sc + 8 * NSC;
+    b.tempty = b.tfull + 8 * NT;
+    b.drain = b.tempty + 8 * NT;
     return b;
 }
 
@@ -113,15 +122,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// 16 int8 -> 16 binary16, exactly: (b ^ 0x80) is b + 128 in [1, 255]; placed
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kSpinLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return;
+}
+
+// int8 pairs -> binary16 pairs, exactly: (b ^ 0x80) = b + 128 in [1, 255];
 // under the exponent byte 0x64 it reads as 1024 + b + 128; minus 1152 gives b.
 __device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t t, uint32_t sel) {
-    uint32_t h = __byte_perm(t, 0x64646464u, sel);
+    const uint32_t h = __byte_perm(t, 0x64646464u, sel);
     uint32_t r;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
     return r;
 }
-__device__ __forceinline__ void convert16(const uint4 v, uint4& lo, uint4& hi) {
+__device__ __forceinline__ void s8x16_to_h16(const uint4 v, uint4& lo, uint4& hi) {
     const uint32_t a = v.x ^ 0x80808080u, b = v.y ^ 0x80808080u;
     const uint32_t c = v.z ^ 0x80808080u, d = v.w ^ 0x80808080u;
     lo = make_uint4(s8x2_to_h2(a, 0x4140), s8x2_to_h2(a, 0x4342),
@@ -129,11 +144,29 @@ __device__ __forceinline__ void convert16(const uint4 v, uint4& lo, uint4& hi) {
     hi = make_uint4(s8x2_to_h2(c, 0x4140), s8x2_to_h2(c, 0x4342),
                     s8x2_to_h2(d, 0x4140), s8x2_to_h2(d, 0x4342));
 }
+// Q4 nibble pairs (stored q + 8 in [0, 15]) -> binary16 pairs: under 0x64 the
+// nibble reads 1024 + s; minus 1032 gives s - 8 = q.
+__device__ __forceinline__ uint32_t u4x2_to_h2(uint32_t nib_bytes, uint32_t sel) {
+    const uint32_t h = __byte_perm(nib_bytes, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+    return r;
+}
 
+struct GroupedArgs {
+    const int32_t* perm;          // sorted position -> pair index
+    const int32_t* offsets;       // [E+1]
+    const int32_t* tile_offsets;  // [E+1] in 128-row tiles
+    int32_t E;
+    int64_t N;                    // per-expert output columns
+};
+
+template <bool kQ4, bool kGrouped>
 __global__ void __launch_bounds__(THREADS, 1)
-tc_gemm_q8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                  const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
-                  float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec4) {
+tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
+               float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec4,
+               GroupedArgs ga, int n_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -142,24 +175,50 @@ tc_gemm_q8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     const int G = (int)(K / kGroup);
-    const int nstages = G / GS;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    constexpr int GB = kQ4 ? 8 : 4;                     // groups per B stage
+    const int na_st = (G + GA - 1) / GA, nb_st = (G + GB - 1) / GB, nsc = (G + SCG - 1) / SCG;
+
+    // ---- tile coordinates ---------------------------------------------------------
+    // m0: first A row (= output row for dense); rows: valid rows in the tile;
+    // n0: first output column; bn0: first B row (expert offset for grouped)
+    int64_t m0, rows, n0, bn0;
+    if constexpr (kGrouped) {
+        const int64_t mt = blockIdx.x / n_tiles;
+        n0 = (int64_t)(blockIdx.x % n_tiles) * BN;
+        if (mt >= ga.tile_offsets[ga.E]) return;        // uniform: whole block leaves
+        int lo = 0, hi = ga.E - 1;                       // last e with tile_offsets[e] <= mt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ga.tile_offsets[mid] <= mt) lo = mid; else hi = mid - 1;
+        }
+        m0 = ga.offsets[lo] + (mt - ga.tile_offsets[lo]) * BM;
+        rows = min64(BM, (int64_t)ga.offsets[lo + 1] - m0);
+        bn0 = (int64_t)lo * ga.N + n0;
+    } else {
+        m0 = (int64_t)blockIdx.y * BM;
+        n0 = (int64_t)blockIdx.x * BN;
+        rows = min64(BM, M - m0);
+        bn0 = n0;
+    }
 
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(B.full_i8 + 8 * i, 1);
-            mbar_init(B.empty_i8 + 8 * i, CONV_WARPS);
+        for (int i = 0; i < NA; ++i) { mbar_init(B.full_a + 8 * i, 1); mbar_init(B.empty_a + 8 * i, 1); }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(B.full_b + 8 * i, 1);
+            mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
         for (int i = 0; i < NF; ++i) {
             mbar_init(B.full_f16 + 8 * i, CONV_WARPS);
             mbar_init(B.empty_f16 + 8 * i, 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSC; ++i) {
             mbar_init(B.full_sc + 8 * i, 1);
             mbar_init(B.ready_sc + 8 * i, CONV_WARPS);
-            mbar_init(B.empty_sc + 8 * i, EPI_THREADS / 32);
+            mbar_init(B.empty_sc + 8 * i, EPI_WARPS);
+        }
+        for (int i = 0; i < NT; ++i) {
             mbar_init(B.tfull + 8 * i, 1);
-            mbar_init(B.tempty + 8 * i, EPI_THREADS / 32);
+            mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
         mbar_init(B.drain, 1);
         *abort = 0;
@@ -183,181 +242,202 @@ tc_gemm_q8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued_i8 = 0, issued_sc = 0;
+            int ia = 0, ib = 0, isc = 0;      // stages issued so far
             bool ok = true;
-            for (int s = 0; s < nstages && ok; ++s) {
-                if (s % 2 == 0) {
-                    const int sc = s / 2;
-                    ok = wait_bar<false>(B.empty_sc + 8 * (sc % 2), ((sc / 2) & 1) ^ 1, abort);
-                    if (!ok) break;
-                    const uint32_t slot = sbase + OFF_SC + (sc % 2) * SC_STAGE;
-                    mbar_expect_tx(B.full_sc + 8 * (sc % 2), SC_DX + SC_DW);
-                    tma_load_2d(slot, &map_dx, sc * SCG, m0, B.full_sc + 8 * (sc % 2));
-                    tma_load_2d(slot + SC_DX, &map_dw, sc * SCG, n0, B.full_sc + 8 * (sc % 2));
-                    issued_sc = sc + 1;
+            // issue in the order the stages are first needed (group index)
+            for (int g = 0; g < G && ok; ++g) {
+                if (g % SCG == 0) {
+                    const int sc = isc, slot = sc % NSC;
+                    if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((sc / NSC) & 1) ^ 1, abort))) break;
+                    const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
+                    mbar_expect_tx(B.full_sc + 8 * slot, SC_DX + SC_DW);
+                    tma_load_2d(dst, &map_dx, sc * SCG, (int32_t)m0, B.full_sc + 8 * slot);
+                    tma_load_2d(dst + SC_DX, &map_dw, sc * SCG, (int32_t)bn0, B.full_sc + 8 * slot);
+                    ++isc;
                 }
-                ok = wait_bar<false>(B.empty_i8 + 8 * (s % NS), ((s / NS) & 1) ^ 1, abort);
-                if (!ok) break;
-                const uint32_t slot = sbase + OFF_I8 + (s % NS) * I8_STAGE;
-                mbar_expect_tx(B.full_i8 + 8 * (s % NS), I8_STAGE);
-                tma_load_2d(slot, &map_a, s * GS * 32, m0, B.full_i8 + 8 * (s % NS));
-                tma_load_2d(slot + I8_A_BYTES, &map_b, s * GS * 32, n0, B.full_i8 + 8 * (s % NS));
-                issued_i8 = s + 1;
+                if (g % GB == 0) {
+                    const int s = ib, slot = s % NB;
+                    if (!(ok = wait_bar<false>(B.empty_b + 8 * slot, ((s / NB) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(B.full_b + 8 * slot, B_STAGE);
+                    tma_load_2d(sbase + OFF_B + slot * B_STAGE, &map_b, s * 128, (int32_t)bn0,
+                                B.full_b + 8 * slot);
+                    ++ib;
+                }
+                if (g % GA == 0) {
+                    const int s = ia, slot = s % NA;
+                    if (!(ok = wait_bar<false>(B.empty_a + 8 * slot, ((s / NA) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
+                    tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, s * 64, (int32_t)m0,
+                                B.full_a + 8 * slot);
+                    ++ia;
+                }
             }
             if (!ok) {
-                // drain: wait (bounded) for the copies this thread issued
-                for (int s = issued_i8 - NS; s < issued_i8; ++s)
-                    if (s >= 0) {
-                        for (uint32_t it = 0; it < kSpinLimit; ++it)
-                            if (mbar_try_wait(B.full_i8 + 8 * (s % NS), (s / NS) & 1)) break;
-                    }
-                for (int sc = issued_sc - 2; sc < issued_sc; ++sc)
-                    if (sc >= 0) {
-                        for (uint32_t it = 0; it < kSpinLimit; ++it)
-                            if (mbar_try_wait(B.full_sc + 8 * (sc % 2), (sc / 2) & 1)) break;
-                    }
+                for (int s = ia - NA; s < ia; ++s)
+                    if (s >= 0) drain_wait(B.full_a + 8 * (s % NA), (s / NA) & 1);
+                for (int s = ib - NB; s < ib; ++s)
+                    if (s >= 0) drain_wait(B.full_b + 8 * (s % NB), (s / NB) & 1);
+                for (int s = isc - NSC; s < isc; ++s)
+                    if (s >= 0) drain_wait(B.full_sc + 8 * (s % NSC), (s / NSC) & 1);
             }
+            (void)na_st; (void)nb_st; (void)nsc;
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool issued_any = false;
             for (int g = 0; g < G; ++g) {
-                const int f = g % NF, b = g % 2;
+                const int sa = g / GA, f = g % NF, b = g % NT;
+                if (!wait_bar<false>(B.full_a + 8 * (sa % NA), (sa / NA) & 1, abort)) break;
                 if (!wait_bar<false>(B.full_f16 + 8 * f, (g / NF) & 1, abort)) break;
-                if (!wait_bar<false>(B.tempty + 8 * b, ((g / 2) & 1) ^ 1, abort)) break;
+                if (!wait_bar<false>(B.tempty + 8 * b, ((g / NT) & 1) ^ 1, abort)) break;
                 tc_fence_after();
-                const uint32_t a_s = sbase + OFF_F16 + f * F16_STAGE;
-                const uint32_t b_s = a_s + F16_A_BYTES;
+                const uint32_t a_s = sbase + OFF_A + (sa % NA) * A_STAGE + (g % GA) * 64;
+                const uint32_t b_s = sbase + OFF_F16 + f * F16_B;
                 const uint32_t d = tmem_base + (uint32_t)(b * BN);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint64_t ad = smem_desc_noswizzle(a_s + j * 256, 128, 512);
-                    const uint64_t bd = smem_desc_noswizzle(b_s + j * 256, 128, 512);
-                    mma_f16(d, ad, bd, IDESC, j);
-                }
+                for (int j = 0; j < 2; ++j)
+                    mma_f16(d, smem_desc_sw128(a_s + j * 32),
+                            smem_desc_noswizzle(b_s + j * 256, 128, 512), IDESC, j);
                 mma_commit(B.empty_f16 + 8 * f);
                 mma_commit(B.tfull + 8 * b);
+                if (g % GA == GA - 1 || g == G - 1) mma_commit(B.empty_a + 8 * (sa % NA));
                 issued_any = true;
             }
             if (*abort && issued_any) {
                 mma_commit(B.drain);
-                for (uint32_t it = 0; it < kSpinLimit; ++it)
-                    if (mbar_try_wait(B.drain, 0)) break;
+                drain_wait(B.drain, 0);
             }
         }
     } else if (warp >= CONV_WARP0) {
         // ------------------------------------------------------------ converters
         const int ct = tid - CONV_WARP0 * 32;
         for (int g = 0; g < G; ++g) {
-            const int gi = g % GS, s = g / GS;
-            if (gi == 0 && !wait_bar<true>(B.full_i8 + 8 * (s % NS), (s / NS) & 1, abort)) break;
+            const int gi = g % GB, s = g / GB;
+            if (gi == 0 && !wait_bar<true>(B.full_b + 8 * (s % NB), (s / NB) & 1, abort)) break;
             if (g % SCG == 0) {
-                const int sc = g / SCG;
-                if (!wait_bar<true>(B.full_sc + 8 * (sc % 2), (sc / 2) & 1, abort)) break;
-                uint8_t* slot = smem + OFF_SC + (sc % 2) * SC_STAGE;
-                const uint16_t* dw_raw = reinterpret_cast<const uint16_t*>(slot + SC_DX);
-                float* dwf = reinterpret_cast<float*>(slot + SC_DX + SC_DW);
+                const int sc = g / SCG, slot = sc % NSC;
+                if (!wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort)) break;
+                uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+                const uint16_t* dw_raw = reinterpret_cast<const uint16_t*>(st + SC_DX);
+                float* dwf = reinterpret_cast<float*>(st + SC_DX + SC_DW);
                 for (int idx = ct; idx < SCG * BN; idx += CONV_THREADS) {
-                    const int gg = idx >> 8, col = idx & (BN - 1);
+                    const int gg = idx >> 7, col = idx & (BN - 1);
                     dwf[gg * BN + col] = half_bits_to_float(dw_raw[col * SCG + gg]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(B.ready_sc + 8 * (sc % 2));
+                if (lane == 0) mbar_arrive(B.ready_sc + 8 * slot);
             }
             const int f = g % NF;
             if (!wait_bar<true>(B.empty_f16 + 8 * f, ((g / NF) & 1) ^ 1, abort)) break;
-            const uint8_t* i8 = smem + OFF_I8 + (s % NS) * I8_STAGE;
-            uint8_t* f16 = smem + OFF_F16 + f * F16_STAGE;
-#pragma unroll 4
-            for (int j = 0; j < (BM + BN) * 2 / CONV_THREADS; ++j) {
-                const int i = ct + j * CONV_THREADS;
-                int row, half;
-                const uint8_t* src_tile;
-                uint8_t* dst_tile;
-                if (i < BM * 2) {
-                    row = i & (BM - 1); half = i >> 7;
-                    src_tile = i8; dst_tile = f16;
-                } else {
-                    const int jj = i - BM * 2;
-                    row = jj & (BN - 1); half = jj >> 8;
-                    src_tile = i8 + I8_A_BYTES; dst_tile = f16 + F16_A_BYTES;
+            const uint8_t* src = smem + OFF_B + (s % NB) * B_STAGE;
+            uint8_t* dst = smem + OFF_F16 + f * F16_B;
+            if constexpr (!kQ4) {
+                // 128 rows x 2 halves (16 int8 each) per group
+#pragma unroll
+                for (int j = 0; j < BN * 2 / CONV_THREADS; ++j) {
+                    const int i = ct + j * CONV_THREADS;
+                    const int row = i & (BN - 1), half = i >> 7;
+                    const int chunk = gi * 2 + half;       // 128-byte swizzle: chunk ^ (row & 7)
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        src + row * 128 + ((chunk ^ (row & 7)) << 4));
+                    uint4 lo, hi;
+                    s8x16_to_h16(v, lo, hi);
+                    uint8_t* o = dst + (row >> 3) * 512 + (half * 2) * 128 + (row & 7) * 16;
+                    *reinterpret_cast<uint4*>(o) = lo;
+                    *reinterpret_cast<uint4*>(o + 128) = hi;
                 }
-                // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-                const int chunk = gi * 2 + half;
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    src_tile + row * 128 + ((chunk ^ (row & 7)) << 4));
-                uint4 lo, hi;
-                convert16(v, lo, hi);
-                uint8_t* dst = dst_tile + (row >> 3) * 512 + (half * 2) * 128 + (row & 7) * 16;
-                *reinterpret_cast<uint4*>(dst) = lo;
-                *reinterpret_cast<uint4*>(dst + 128) = hi;
+            } else {
+                // 128 rows x one 16-byte group (32 nibbles) per group
+#pragma unroll
+                for (int j = 0; j < BN / CONV_THREADS; ++j) {
+                    const int row = ct + j * CONV_THREADS;
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        src + row * 128 + ((gi ^ (row & 7)) << 4));
+                    // byte j: element j (low nibble), element j+16 (high nibble)
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t lo_h[8], hi_h[8];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+                        lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+                        lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+                        hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+                        hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+                    }
+                    uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
+                    *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+                    *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+                    *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+                    *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(B.full_f16 + 8 * f);
-                if (gi == GS - 1) mbar_arrive(B.empty_i8 + 8 * (s % NS));
+                if (gi == GB - 1 || g == G - 1) mbar_arrive(B.empty_b + 8 * (s % NB));
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int wg = tid >> 7, q = warp & 3;
+        const int wg = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
-        const int cb = wg * 128;
-        float acc[128];
+        const int cb = wg * 64;
+        uint64_t acc[32];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 32; ++i) acc[i] = 0ull;
         bool ok = true;
         for (int g = 0; g < G && ok; ++g) {
-            const int sc = g / SCG, b = g % 2;
-            if (g % SCG == 0) ok = wait_bar<true>(B.ready_sc + 8 * (sc % 2), (sc / 2) & 1, abort);
+            const int sc = g / SCG, slot = sc % NSC, b = g % NT;
+            if (g % SCG == 0) ok = wait_bar<true>(B.ready_sc + 8 * slot, (sc / NSC) & 1, abort);
             if (!ok) break;
-            ok = wait_bar<true>(B.tfull + 8 * b, (g / 2) & 1, abort);
+            ok = wait_bar<true>(B.tfull + 8 * b, (g / NT) & 1, abort);
             if (!ok) break;
             tc_fence_after();
-            const uint8_t* slot = smem + OFF_SC + (sc % 2) * SC_STAGE;
-            const float dxv = reinterpret_cast<const float*>(slot)[row * SCG + (g % SCG)];
-            const float* dwf = reinterpret_cast<const float*>(slot + SC_DX + SC_DW) +
-                               (g % SCG) * BN + cb;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cb);
+            uint32_t s[64];
+            tmem_ld32(taddr, s);
+            tmem_ld32(taddr + 32, s + 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.tempty + 8 * b);
+            const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+            const float dxv = reinterpret_cast<const float*>(st)[row * SCG + (g % SCG)];
+            const uint64_t dx2 = pack2(dxv, dxv);
+            const float* dwf = reinterpret_cast<const float*>(st + SC_DX + SC_DW) +
+                               (g % SCG) * BN + cb;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t s[16];
-                tmem_ld16(taddr + c * 16, s);
-                tmem_wait_ld();
-                if (c == 7) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B.tempty + 8 * b);
-                }
-#pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
-                    const float4 w = *reinterpret_cast<const float4*>(dwf + c * 16 + i4 * 4);
-                    const int o = c * 16 + i4 * 4;
-                    acc[o + 0] = fmaf(__uint_as_float(s[i4 * 4 + 0]), dxv * w.x, acc[o + 0]);
-                    acc[o + 1] = fmaf(__uint_as_float(s[i4 * 4 + 1]), dxv * w.y, acc[o + 1]);
-                    acc[o + 2] = fmaf(__uint_as_float(s[i4 * 4 + 2]), dxv * w.z, acc[o + 2]);
-                    acc[o + 3] = fmaf(__uint_as_float(s[i4 * 4 + 3]), dxv * w.w, acc[o + 3]);
-                }
+            for (int i = 0; i < 16; ++i) {
+                const float4 w = *reinterpret_cast<const float4*>(dwf + i * 4);
+                fma2_scaled(acc[2 * i], s[4 * i], s[4 * i + 1], w.x, w.y, dx2);
+                fma2_scaled(acc[2 * i + 1], s[4 * i + 2], s[4 * i + 3], w.z, w.w, dx2);
             }
-            if (g % SCG == SCG - 1) {
+            if (g % SCG == SCG - 1 || g == G - 1) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(B.empty_sc + 8 * (sc % 2));
+                if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
             }
         }
-        if (ok && m0 + row < M) {
-            float* yr = y + (int64_t)(m0 + row) * ldy + n0 + cb;
+        if (ok && row < rows) {
+            int64_t orow;
+            if constexpr (kGrouped) orow = ga.perm[m0 + row];
+            else orow = m0 + row;
+            float* yr = y + orow * ldy + n0 + cb;
             const int64_t ncols = N - (n0 + cb);
-            if (vec4 && ncols >= 128) {
+            if (vec4 && ncols >= 64) {
 #pragma unroll
-                for (int i = 0; i < 128; i += 4)
-                    *reinterpret_cast<float4*>(yr + i) =
-                        make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                for (int i = 0; i < 16; ++i) {
+                    const float2 a = unpack2(acc[2 * i]), c = unpack2(acc[2 * i + 1]);
+                    *reinterpret_cast<float4*>(yr + 4 * i) = make_float4(a.x, a.y, c.x, c.y);
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (i < ncols) yr[i] = acc[i];
+                for (int i = 0; i < 32; ++i) {
+                    const float2 a = unpack2(acc[i]);
+                    if (2 * i < ncols) yr[2 * i] = a.x;
+                    if (2 * i + 1 < ncols) yr[2 * i + 1] = a.y;
+                }
             }
         }
     }
@@ -367,6 +447,37 @@ tc_gemm_q8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- pre-pass: int8 codes -> binary16 (optionally gathered) ---------------------------
+
+// Dense: a16[r] = fp16(qx[r]).  Grouped (perm != nullptr): sorted position i
+// takes activation row x_row(perm[i]); its scales are gathered into dxg too.
+__global__ void __launch_bounds__(256)
+widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, int64_t rows,
+                  int64_t K, __half* __restrict__ a16, float* __restrict__ dxg,
+                  const int32_t* __restrict__ perm, const int32_t* __restrict__ n_rows,
+                  int32_t topk, int32_t x_row_mode) {
+    const int64_t chunks = K / 16;                   // 16 codes per thread step
+    const int64_t G = K / kGroup;
+    const int64_t limit = n_rows ? (int64_t)*n_rows : rows;
+    const int64_t total = limit * chunks;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / chunks, c = i % chunks;
+        int64_t src = r;
+        if (perm) {
+            const int32_t p = perm[r];
+            src = x_row_mode ? p : p / topk;
+        }
+        const uint4 v = *reinterpret_cast<const uint4*>(qx + src * K + c * 16);
+        uint4 lo, hi;
+        s8x16_to_h16(v, lo, hi);
+        uint4* o = reinterpret_cast<uint4*>(a16 + r * K + c * 16);
+        o[0] = lo;
+        o[1] = hi;
+        if (dxg && c % 2 == 0) dxg[r * G + c / 2] = dx[src * G + c / 2];
     }
 }
 
@@ -406,6 +517,46 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
+// dx [rows][G], dw [brows][G].
+bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
+               const void* a16, const void* qw, const float* dx, const uint16_t* dw,
+               int64_t rows, int64_t brows, int64_t K, bool q4) {
+    const int64_t G = K / kGroup;
+    const int64_t wbytes = q4 ? K / 2 : K;
+    return make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_UINT16, dw, G, brows, G * 2, SCG, BN,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <bool kQ4, bool kGrouped>
+cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& mb,
+                          const CUtensorMap& mdx, const CUtensorMap& mdw, float* y, int64_t M,
+                          int64_t N, int64_t K, int64_t ldy, GroupedArgs ga, int n_tiles,
+                          cudaStream_t s) {
+    cudaError_t e = ensure_smem_attr((const void*)tc_gemm_kernel<kQ4, kGrouped>, SMEM_BYTES,
+                                     9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
+    if (e != cudaSuccess) return e;
+    const bool vec4 = ((uintptr_t)y % 16 == 0) && (ldy % 4 == 0);
+    tc_gemm_kernel<kQ4, kGrouped><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
+                                                                    ldy, vec4, ga, n_tiles);
+    return cudaGetLastError();
+}
+
+int widen_grid(int64_t work) {
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+size_t align16(size_t v) { return (v + 15) / 16 * 16; }
+
 }  // namespace
 
 bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const void* dw) {
@@ -414,26 +565,22 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const vo
            encoder() != nullptr;
 }
 
+size_t tc_gemm_workspace(int64_t M, int64_t K) { return align16((size_t)M * K * 2); }
+
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
-                           const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
-                           cudaStream_t s) {
-    const int64_t G = K / kGroup;
-    CUtensorMap ma, mb, mdx, mdw;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, qx, K, M, K, 128, BM,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, K, 128, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, M, G * 4, SCG, BM,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&mdw, CU_TENSOR_MAP_DATA_TYPE_UINT16, dw, G, N, G * 2, SCG, BN,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr((const void*)tc_gemm_q8_kernel, SMEM_BYTES, 9);
+                           const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
+                           void* workspace, cudaStream_t s) {
+    __half* a16 = static_cast<__half*>(workspace);
+    widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
+                                                               nullptr, 1, 0);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const bool vec4 = ((uintptr_t)y % 16 == 0) && (ldy % 4 == 0);
+    CUtensorMap ma, mb, mdx, mdw;
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dw, M, N, K, q4)) return cudaErrorInvalidValue;
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    tc_gemm_q8_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K, ldy, vec4);
-    return cudaGetLastError();
+    GroupedArgs ga{};
+    return q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, 0, s)
+              : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, 0, s);
 }
 
 unsigned int read_and_clear_tc_error() {

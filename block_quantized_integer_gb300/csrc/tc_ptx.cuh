@@ -100,6 +100,57 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr) : "memory");
 }
 
+// 32 lanes x 32 bits, 32 consecutive columns
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr) : "memory");
+}
+
+// y2 (two binary32 in one 64-bit register) += {s0, s1} * ({w0, w1} * dx2)
+__device__ __forceinline__ void fma2_scaled(uint64_t& y2, uint32_t s0, uint32_t s1, float w0,
+                                            float w1, uint64_t dx2) {
+    asm("{\n\t.reg .b64 s, w, p;\n\t"
+        "mov.b64 s, {%1, %2};\n\t"
+        "mov.b64 w, {%3, %4};\n\t"
+        "mul.rn.f32x2 p, w, %5;\n\t"
+        "fma.rn.f32x2 %0, s, p, %0;\n\t}"
+        : "+l"(y2) : "r"(s0), "r"(s1), "f"(w0), "f"(w1), "l"(dx2));
+}
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle (the layout a TMA
+// load with CU_TENSOR_MAP_SWIZZLE_128B writes for 128-byte rows): 8-row atoms
+// of 1024 bytes (sbo = 1024), lbo unused; the start address may move along K
+// inside the 128-byte row (+32 bytes per 16 binary16 elements).  Layout type
+// SWIZZLE_128B = 2 at [61,64), version 1 at [46,48).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                    // lbo (ignored for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;          // sbo: 8 rows x 128 bytes
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor, K-major, no swizzle ("interleaved" core
 // matrices of 8 rows x 16 bytes stored as 128 contiguous bytes):
 //   lbo = byte distance between core matrices adjacent along K,

@@ -61,7 +61,7 @@ typedef enum {
     QG_ALGO_AUTO = 0,
     QG_ALGO_GEMV = 1,     /* split-K GEMV on dp4a, M <= 8 (decode) */
     QG_ALGO_MMA = 2,      /* warp-level mma.sync int8 tile GEMM, any M */
-    QG_ALGO_TCGEN05 = 3   /* tcgen05 tensor-memory GEMM, prefill (large M) */
+    QG_ALGO_TCGEN05 = 3   /* tcgen05 tensor-memory GEMM, prefill; K % 256 == 0, needs workspace */
 } qg_algo;
 
 /* Workspace sizing: op is one of the QG_OP_* values. */
@@ -71,8 +71,10 @@ enum { QG_OP_QGEMM_Q8_0 = 1, QG_OP_QGEMM_Q4_0 = 2, QG_OP_GROUPED_MOE = 3 };
 const char* qg_status_string(qg_status s);
 
 /* Bytes of device workspace the given call needs (0 if none).  For the dense
- * GEMMs pass M, N, K (T, topk, E ignored); for the MoE GEMM pass K and N and
- * the routing sizes T, topk, E (M ignored). */
+ * GEMMs pass M, N, K (T, topk, E ignored): M > 8 with K % 256 == 0 runs on the
+ * tensor cores and needs M * K * 2 bytes (the activation codes widened to
+ * binary16).  For the MoE GEMM pass K and N and the routing sizes T, topk, E
+ * (M ignored).  Workspace pointers must be 16-byte aligned. */
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,
                             int64_t T, int32_t topk, int32_t E);
 
@@ -103,7 +105,8 @@ qg_status quantize_weight_q4_0(const float* w, int64_t N, int64_t K,
  * y = sum_g dw * dx * S as above, every S formed exactly before it is scaled,
  * the sum over groups in binary32 (order depends on the kernel; fixed for a
  * given shape and algo, so results are run-to-run deterministic).
- * workspace: pass NULL/0 when qgemm_workspace_size() returns 0. */
+ * workspace: at least qgemm_workspace_size() bytes (QG_ERR_WORKSPACE if
+ * smaller); NULL/0 when that size is 0. */
 qg_status qgemm_q8_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                      const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);

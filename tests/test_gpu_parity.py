@@ -86,8 +86,6 @@ def _gemm(bits, algo, qx, dx, qw, dw, y=None):
 @pytest.mark.parametrize("bits", [8, 4])
 def test_group_dots_exact(algo, bits):
     """With dx = 1 and dw = 1 on group g and 0 elsewhere, y = S[:, :, g] exactly."""
-    if algo == qg.ALGO_TCGEN05 and bits == 4:
-        pytest.skip("the tcgen05 dense kernel takes Q8_0 weights")
     M = 5 if algo == qg.ALGO_GEMV else 70
     N, K = (150, 256) if algo != qg.ALGO_TCGEN05 else (300, 512)
     G = K // 32
@@ -139,8 +137,6 @@ TC_SHAPES = [(4, 256, 512), (128, 256, 256), (300, 130, 768), (129, 513, 1024), 
                          [(qg.ALGO_MMA,) + s for s in MMA_SHAPES] +
                          [(qg.ALGO_TCGEN05,) + s for s in TC_SHAPES])
 def test_qgemm_parity(algo, M, N, K, bits):
-    if algo == qg.ALGO_TCGEN05 and bits == 4:
-        pytest.skip("the tcgen05 dense kernel takes Q8_0 weights")
     qx, dx, qw, dw = _case(M, N, K, bits, M * 7 + N * 3 + K + bits)
     y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
     y = _gemm(bits, algo, to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
@@ -209,7 +205,7 @@ def test_decode_full_shape(decode_weights, shape, M):
 
 # ------------------------------------------------------------------ full-size prefill (sampled)
 
-@pytest.mark.parametrize("algo", [qg.ALGO_AUTO, qg.ALGO_TCGEN05, qg.ALGO_MMA])
+@pytest.mark.parametrize("algo", [qg.ALGO_AUTO, qg.ALGO_MMA])
 @pytest.mark.parametrize("shape", inputs.PREFILL_SHAPES)
 def test_prefill_full_shape_sampled(shape, algo):
     M, N, K = shape
