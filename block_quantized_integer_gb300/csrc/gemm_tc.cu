@@ -46,11 +46,10 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 128;
-constexpr int GA = 2;                  // groups per A stage (64 binary16 = 128-byte rows)
+constexpr int GA = 2;                  // groups per A stage = one pair (64 binary16 = 128-byte rows)
 constexpr int NA = 5;                  // A stages
 constexpr int NB = 4;                  // B stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
-constexpr int NF = 4;                  // binary16 B buffers (one group each)
-constexpr int NT = 4;                  // TMEM accumulator buffers (128 columns each)
+constexpr int NP = 2;                  // pair slots (binary16 B buffers and TMEM accumulators)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int THREADS = 384;
@@ -59,7 +58,8 @@ constexpr int CONV_WARP0 = 10, CONV_WARPS = 2, CONV_THREADS = CONV_WARPS * 32;
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
-constexpr int F16_B = BN * 32 * 2;                   // 8192
+constexpr int F16_B = BN * 32 * 2;                   // 8192: one group of binary16 B
+constexpr int F16_PAIR = 2 * F16_B;                  // 16384
 constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128][8] f32
 constexpr int SC_DW = BN * SCG * 2;                  // 2048: dw [128][8] f16
 constexpr int SC_DWF = SCG * BN * 4;                 // 4096: dw [8][128] f32
@@ -68,21 +68,21 @@ constexpr int SC_STAGE = SC_DX + SC_DW + SC_DWF;     // 10240
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NA * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
-constexpr int OFF_SC = OFF_F16 + NF * F16_B;
+constexpr int OFF_SC = OFF_F16 + NP * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 2 * NA + 2 * NB + 2 * NF + 3 * NSC + 2 * NT + 1;
+constexpr int NUM_BARS = 2 * NA + 2 * NB + 3 * NP + 3 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 KiB alignment");
 
-constexpr uint32_t TMEM_COLS = NT * BN;               // 512
+constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of two groups
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 struct Bars {
-    uint32_t full_a, empty_a, full_b, empty_b, full_f16, empty_f16, full_sc, ready_sc, empty_sc,
-        tfull, tempty, drain;
+    uint32_t full_a, empty_a, full_b, empty_b, full_f16, tfull, tempty, full_sc, ready_sc,
+        empty_sc, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
@@ -92,13 +92,12 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     b.full_b = b.empty_a + 8 * NA;
     b.empty_b = b.full_b + 8 * NB;
     b.full_f16 = b.empty_b + 8 * NB;
-    b.empty_f16 = b.full_f16 + 8 * NF;
-    b.full_sc = b.empty_f16 + 8 * NF;
+    b.tfull = b.full_f16 + 8 * NP;
+    b.tempty = b.tfull + 8 * NP;
+    b.full_sc = b.tempty + 8 * NP;
     b.ready_sc = b.full_sc + 8 * NSC;
     b.empty_sc = b.ready_sc + 8 * NSC;
-    b.tfull = b.empty_sc + 8 * NSC;
-    b.tempty = b.tfull + 8 * NT;
-    b.drain = b.tempty + 8 * NT;
+    b.drain = b.empty_sc + 8 * NSC;
     return b;
 }
 
@@ -153,6 +152,49 @@ __device__ __forceinline__ uint32_t u4x2_to_h2(uint32_t nib_bytes, uint32_t sel)
     return r;
 }
 
+// Group gi (0 .. GB-1) of the int8 / packed 4-bit B stage -> binary16 B buffer
+// (canonical no-swizzle K-major layout: core matrix (row/8, k8) at
+// (row/8)*512 + k8*128, row%8 at +16 each).
+template <bool kQ4>
+__device__ __forceinline__ void convert_group(const uint8_t* src, uint8_t* dst, int gi, int ct) {
+    if constexpr (!kQ4) {
+#pragma unroll
+        for (int j = 0; j < BN * 2 / CONV_THREADS; ++j) {
+            const int i = ct + j * CONV_THREADS;
+            const int row = i & (BN - 1), half = i >> 7;
+            const int chunk = gi * 2 + half;          // 128-byte swizzle: chunk ^ (row & 7)
+            const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((chunk ^ (row & 7)) << 4));
+            uint4 lo, hi;
+            s8x16_to_h16(v, lo, hi);
+            uint8_t* o = dst + (row >> 3) * 512 + (half * 2) * 128 + (row & 7) * 16;
+            *reinterpret_cast<uint4*>(o) = lo;
+            *reinterpret_cast<uint4*>(o + 128) = hi;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < BN / CONV_THREADS; ++j) {
+            const int row = ct + j * CONV_THREADS;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((gi ^ (row & 7)) << 4));
+            // byte j: element j (low nibble), element j+16 (high nibble)
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t lo_h[8], hi_h[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+                lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+                lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+                hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+                hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+            }
+            uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
+            *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+            *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+            *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+            *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+        }
+    }
+}
+
 struct GroupedArgs {
     const int32_t* perm;          // sorted position -> pair index
     const int32_t* offsets;       // [E+1]
@@ -161,12 +203,40 @@ struct GroupedArgs {
     int64_t N;                    // per-expert output columns
 };
 
+struct Tile {
+    int64_t m0, rows, n0, bn0;    // first A row, valid rows, first column, first B row
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, const GroupedArgs& ga, int n_tiles) {
+    Tile T;
+    const int64_t mt = t / n_tiles;
+    T.n0 = (t % n_tiles) * BN;
+    if constexpr (kGrouped) {
+        int lo = 0, hi = ga.E - 1;                       // last e with tile_offsets[e] <= mt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ga.tile_offsets[mid] <= mt) lo = mid; else hi = mid - 1;
+        }
+        T.m0 = ga.offsets[lo] + (mt - ga.tile_offsets[lo]) * BM;
+        T.rows = min64(BM, (int64_t)ga.offsets[lo + 1] - T.m0);
+        T.bn0 = (int64_t)lo * ga.N + T.n0;
+    } else {
+        T.m0 = mt * BM;
+        T.rows = min64(BM, M - T.m0);
+        T.bn0 = T.n0;
+    }
+    return T;
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ...  All roles walk the same
+// tile sequence; ring positions and barrier phases run on across tiles.
 template <bool kQ4, bool kGrouped>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
                float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec4,
-               GroupedArgs ga, int n_tiles) {
+               GroupedArgs ga, int n_tiles, int64_t dense_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -174,32 +244,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const Bars B = bars_at(sbase + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-    const int G = (int)(K / kGroup);
-    constexpr int GB = kQ4 ? 8 : 4;                     // groups per B stage
-    const int na_st = (G + GA - 1) / GA, nb_st = (G + GB - 1) / GB, nsc = (G + SCG - 1) / SCG;
-
-    // ---- tile coordinates ---------------------------------------------------------
-    // m0: first A row (= output row for dense); rows: valid rows in the tile;
-    // n0: first output column; bn0: first B row (expert offset for grouped)
-    int64_t m0, rows, n0, bn0;
-    if constexpr (kGrouped) {
-        const int64_t mt = blockIdx.x / n_tiles;
-        n0 = (int64_t)(blockIdx.x % n_tiles) * BN;
-        if (mt >= ga.tile_offsets[ga.E]) return;        // uniform: whole block leaves
-        int lo = 0, hi = ga.E - 1;                       // last e with tile_offsets[e] <= mt
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (ga.tile_offsets[mid] <= mt) lo = mid; else hi = mid - 1;
-        }
-        m0 = ga.offsets[lo] + (mt - ga.tile_offsets[lo]) * BM;
-        rows = min64(BM, (int64_t)ga.offsets[lo + 1] - m0);
-        bn0 = (int64_t)lo * ga.N + n0;
-    } else {
-        m0 = (int64_t)blockIdx.y * BM;
-        n0 = (int64_t)blockIdx.x * BN;
-        rows = min64(BM, M - m0);
-        bn0 = n0;
-    }
+    const int G = (int)(K / kGroup);                    // multiple of 8
+    const int PAIRS = G / 2;
+    constexpr int GB = kQ4 ? 8 : 4;                      // groups per B stage
+    const int64_t num_tiles = kGrouped ? (int64_t)ga.tile_offsets[ga.E] * n_tiles : dense_tiles;
+    const int64_t t0 = blockIdx.x, dt = gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < NA; ++i) { mbar_init(B.full_a + 8 * i, 1); mbar_init(B.empty_a + 8 * i, 1); }
@@ -207,18 +256,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NF; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(B.full_f16 + 8 * i, CONV_WARPS);
-            mbar_init(B.empty_f16 + 8 * i, 1);
+            mbar_init(B.tfull + 8 * i, 1);
+            mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
         for (int i = 0; i < NSC; ++i) {
             mbar_init(B.full_sc + 8 * i, 1);
             mbar_init(B.ready_sc + 8 * i, CONV_WARPS);
             mbar_init(B.empty_sc + 8 * i, EPI_WARPS);
-        }
-        for (int i = 0; i < NT; ++i) {
-            mbar_init(B.tfull + 8 * i, 1);
-            mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
         mbar_init(B.drain, 1);
         *abort = 0;
@@ -242,67 +288,80 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int ia = 0, ib = 0, isc = 0;      // stages issued so far
+            int64_t ia = 0, ib = 0, isc = 0;      // stages issued so far (run on across tiles)
             bool ok = true;
-            // issue in the order the stages are first needed (group index)
-            for (int g = 0; g < G && ok; ++g) {
-                if (g % SCG == 0) {
-                    const int sc = isc, slot = sc % NSC;
-                    if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((sc / NSC) & 1) ^ 1, abort))) break;
-                    const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
-                    mbar_expect_tx(B.full_sc + 8 * slot, SC_DX + SC_DW);
-                    tma_load_2d(dst, &map_dx, sc * SCG, (int32_t)m0, B.full_sc + 8 * slot);
-                    tma_load_2d(dst + SC_DX, &map_dw, sc * SCG, (int32_t)bn0, B.full_sc + 8 * slot);
-                    ++isc;
-                }
-                if (g % GB == 0) {
-                    const int s = ib, slot = s % NB;
-                    if (!(ok = wait_bar<false>(B.empty_b + 8 * slot, ((s / NB) & 1) ^ 1, abort))) break;
-                    mbar_expect_tx(B.full_b + 8 * slot, B_STAGE);
-                    tma_load_2d(sbase + OFF_B + slot * B_STAGE, &map_b, s * 128, (int32_t)bn0,
-                                B.full_b + 8 * slot);
-                    ++ib;
-                }
-                if (g % GA == 0) {
-                    const int s = ia, slot = s % NA;
-                    if (!(ok = wait_bar<false>(B.empty_a + 8 * slot, ((s / NA) & 1) ^ 1, abort))) break;
-                    mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
-                    tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, s * 64, (int32_t)m0,
-                                B.full_a + 8 * slot);
-                    ++ia;
+            for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+                const Tile T = tile_at<kGrouped>(t, M, ga, n_tiles);
+                // issue in the order the stages are first needed
+                for (int g = 0; g < G && ok; ++g) {
+                    if (g % SCG == 0) {
+                        const int slot = (int)(isc % NSC);
+                        if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
+                        const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
+                        mbar_expect_tx(B.full_sc + 8 * slot, SC_DX + SC_DW);
+                        tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
+                        tma_load_2d(dst + SC_DX, &map_dw, g, (int32_t)T.bn0, B.full_sc + 8 * slot);
+                        ++isc;
+                    }
+                    if (g % GB == 0) {
+                        const int slot = (int)(ib % NB);
+                        if (!(ok = wait_bar<false>(B.empty_b + 8 * slot, ((ib / NB) & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(B.full_b + 8 * slot, B_STAGE);
+                        tma_load_2d(sbase + OFF_B + slot * B_STAGE, &map_b, (g / GB) * 128,
+                                    (int32_t)T.bn0, B.full_b + 8 * slot);
+                        ++ib;
+                    }
+                    if (g % GA == 0) {
+                        const int slot = (int)(ia % NA);
+                        if (!(ok = wait_bar<false>(B.empty_a + 8 * slot, ((ia / NA) & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
+                        tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, g * 32, (int32_t)T.m0,
+                                    B.full_a + 8 * slot);
+                        ++ia;
+                    }
                 }
             }
             if (!ok) {
-                for (int s = ia - NA; s < ia; ++s)
+                for (int64_t s = ia - NA; s < ia; ++s)
                     if (s >= 0) drain_wait(B.full_a + 8 * (s % NA), (s / NA) & 1);
-                for (int s = ib - NB; s < ib; ++s)
+                for (int64_t s = ib - NB; s < ib; ++s)
                     if (s >= 0) drain_wait(B.full_b + 8 * (s % NB), (s / NB) & 1);
-                for (int s = isc - NSC; s < isc; ++s)
+                for (int64_t s = isc - NSC; s < isc; ++s)
                     if (s >= 0) drain_wait(B.full_sc + 8 * (s % NSC), (s / NSC) & 1);
             }
-            (void)na_st; (void)nb_st; (void)nsc;
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool issued_any = false;
-            for (int g = 0; g < G; ++g) {
-                const int sa = g / GA, f = g % NF, b = g % NT;
-                if (!wait_bar<false>(B.full_a + 8 * (sa % NA), (sa / NA) & 1, abort)) break;
-                if (!wait_bar<false>(B.full_f16 + 8 * f, (g / NF) & 1, abort)) break;
-                if (!wait_bar<false>(B.tempty + 8 * b, ((g / NT) & 1) ^ 1, abort)) break;
-                tc_fence_after();
-                const uint32_t a_s = sbase + OFF_A + (sa % NA) * A_STAGE + (g % GA) * 64;
-                const uint32_t b_s = sbase + OFF_F16 + f * F16_B;
-                const uint32_t d = tmem_base + (uint32_t)(b * BN);
+            bool issued_any = false, ok = true;
+            int64_t p = 0;                                  // pair counter (A stage = pair)
+            for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                    const int sa = (int)(p % NA), ps = (int)(p % NP);
+                    const uint32_t pa = (uint32_t)((p / NA) & 1), pp = (uint32_t)((p / NP) & 1);
+                    // the three probes go out back to back; one branch on all of them
+                    const bool ready = mbar_try_wait(B.full_a + 8 * sa, pa) &
+                                       mbar_try_wait(B.full_f16 + 8 * ps, pp) &
+                                       mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
+                    if (!ready) {
+                        if (!(ok = wait_bar<false>(B.full_a + 8 * sa, pa, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * ps, pp, abort))) break;
+                        if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = sbase + OFF_A + sa * A_STAGE;
+                    const uint32_t b_s = sbase + OFF_F16 + ps * F16_PAIR;
+                    const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    mma_f16(d, smem_desc_sw128(a_s + j * 32),
-                            smem_desc_noswizzle(b_s + j * 256, 128, 512), IDESC, j);
-                mma_commit(B.empty_f16 + 8 * f);
-                mma_commit(B.tfull + 8 * b);
-                if (g % GA == GA - 1 || g == G - 1) mma_commit(B.empty_a + 8 * (sa % NA));
-                issued_any = true;
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
+                                    smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
+                    mma_commit(B.tfull + 8 * ps);
+                    mma_commit(B.empty_a + 8 * sa);
+                    issued_any = true;
+                }
             }
             if (*abort && issued_any) {
                 mma_commit(B.drain);
@@ -312,71 +371,40 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     } else if (warp >= CONV_WARP0) {
         // ------------------------------------------------------------ converters
         const int ct = tid - CONV_WARP0 * 32;
-        for (int g = 0; g < G; ++g) {
-            const int gi = g % GB, s = g / GB;
-            if (gi == 0 && !wait_bar<true>(B.full_b + 8 * (s % NB), (s / NB) & 1, abort)) break;
-            if (g % SCG == 0) {
-                const int sc = g / SCG, slot = sc % NSC;
-                if (!wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort)) break;
-                uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                const uint16_t* dw_raw = reinterpret_cast<const uint16_t*>(st + SC_DX);
-                float* dwf = reinterpret_cast<float*>(st + SC_DX + SC_DW);
-                for (int idx = ct; idx < SCG * BN; idx += CONV_THREADS) {
-                    const int gg = idx >> 7, col = idx & (BN - 1);
-                    dwf[gg * BN + col] = half_bits_to_float(dw_raw[col * SCG + gg]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.ready_sc + 8 * slot);
-            }
-            const int f = g % NF;
-            if (!wait_bar<true>(B.empty_f16 + 8 * f, ((g / NF) & 1) ^ 1, abort)) break;
-            const uint8_t* src = smem + OFF_B + (s % NB) * B_STAGE;
-            uint8_t* dst = smem + OFF_F16 + f * F16_B;
-            if constexpr (!kQ4) {
-                // 128 rows x 2 halves (16 int8 each) per group
-#pragma unroll
-                for (int j = 0; j < BN * 2 / CONV_THREADS; ++j) {
-                    const int i = ct + j * CONV_THREADS;
-                    const int row = i & (BN - 1), half = i >> 7;
-                    const int chunk = gi * 2 + half;       // 128-byte swizzle: chunk ^ (row & 7)
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        src + row * 128 + ((chunk ^ (row & 7)) << 4));
-                    uint4 lo, hi;
-                    s8x16_to_h16(v, lo, hi);
-                    uint8_t* o = dst + (row >> 3) * 512 + (half * 2) * 128 + (row & 7) * 16;
-                    *reinterpret_cast<uint4*>(o) = lo;
-                    *reinterpret_cast<uint4*>(o + 128) = hi;
-                }
-            } else {
-                // 128 rows x one 16-byte group (32 nibbles) per group
-#pragma unroll
-                for (int j = 0; j < BN / CONV_THREADS; ++j) {
-                    const int row = ct + j * CONV_THREADS;
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        src + row * 128 + ((gi ^ (row & 7)) << 4));
-                    // byte j: element j (low nibble), element j+16 (high nibble)
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t lo_h[8], hi_h[8];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
-                        lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
-                        lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
-                        hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
-                        hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+        int64_t p = 0, sb = 0, sc = 0;                      // run on across tiles
+        bool ok = true;
+        for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+            for (int pl = 0; pl < PAIRS && ok; ++pl, ++p) {
+                const int g0 = 2 * pl;
+                if (g0 % GB == 0 && !(ok = wait_bar<true>(B.full_b + 8 * (sb % NB), (sb / NB) & 1, abort))) break;
+                if (g0 % SCG == 0) {
+                    const int slot = (int)(sc % NSC);
+                    if (!(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                    uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+                    const uint16_t* dw_raw = reinterpret_cast<const uint16_t*>(st + SC_DX);
+                    float* dwf = reinterpret_cast<float*>(st + SC_DX + SC_DW);
+                    for (int idx = ct; idx < SCG * BN; idx += CONV_THREADS) {
+                        const int gg = idx >> 7, col = idx & (BN - 1);
+                        dwf[gg * BN + col] = half_bits_to_float(dw_raw[col * SCG + gg]);
                     }
-                    uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
-                    *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
-                    *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
-                    *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
-                    *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.ready_sc + 8 * slot);
+                    ++sc;
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(B.full_f16 + 8 * f);
-                if (gi == GB - 1 || g == G - 1) mbar_arrive(B.empty_b + 8 * (s % NB));
+                // the pair slot is free once the MMAs of pair p - NP completed
+                const int ps = (int)(p % NP);
+                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)(((p / NP) & 1) ^ 1), abort))) break;
+                const uint8_t* src = smem + OFF_B + (sb % NB) * B_STAGE;
+                uint8_t* dst = smem + OFF_F16 + ps * F16_PAIR;
+                convert_group<kQ4>(src, dst, g0 % GB, ct);
+                convert_group<kQ4>(src, dst + F16_B, (g0 + 1) % GB, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(B.full_f16 + 8 * ps);
+                    if ((g0 + 1) % GB == GB - 1) mbar_arrive(B.empty_b + 8 * (sb % NB));
+                }
+                if ((g0 + 1) % GB == GB - 1) ++sb;
             }
         }
     } else {
@@ -384,59 +412,70 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const int wg = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
         const int cb = wg * 64;
-        uint64_t acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0ull;
+        uint32_t p = 0, sc = 0;
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
-            const int sc = g / SCG, slot = sc % NSC, b = g % NT;
-            if (g % SCG == 0) ok = wait_bar<true>(B.ready_sc + 8 * slot, (sc / NSC) & 1, abort);
-            if (!ok) break;
-            ok = wait_bar<true>(B.tfull + 8 * b, (g / NT) & 1, abort);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cb);
-            uint32_t s[64];
-            tmem_ld32(taddr, s);
-            tmem_ld32(taddr + 32, s + 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.tempty + 8 * b);
-            const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-            const float dxv = reinterpret_cast<const float*>(st)[row * SCG + (g % SCG)];
-            const uint64_t dx2 = pack2(dxv, dxv);
-            const float* dwf = reinterpret_cast<const float*>(st + SC_DX + SC_DW) +
-                               (g % SCG) * BN + cb;
+        for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+            uint64_t acc[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 w = *reinterpret_cast<const float4*>(dwf + i * 4);
-                fma2_scaled(acc[2 * i], s[4 * i], s[4 * i + 1], w.x, w.y, dx2);
-                fma2_scaled(acc[2 * i + 1], s[4 * i + 2], s[4 * i + 3], w.z, w.w, dx2);
-            }
-            if (g % SCG == SCG - 1 || g == G - 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
-            }
-        }
-        if (ok && row < rows) {
-            int64_t orow;
-            if constexpr (kGrouped) orow = ga.perm[m0 + row];
-            else orow = m0 + row;
-            float* yr = y + orow * ldy + n0 + cb;
-            const int64_t ncols = N - (n0 + cb);
-            if (vec4 && ncols >= 64) {
+            for (int i = 0; i < 32; ++i) acc[i] = 0ull;
+            for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                const int g0 = 2 * pl, ps = (int)(p % NP);
+                const int slot = (int)(sc % NSC);
+                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.ready_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)((p / NP) & 1), abort))) break;
+                tc_fence_after();
+                const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)(ps * 2 * BN + h * BN + cb);
+                    uint32_t s[64];
+                    tmem_ld32(taddr, s);
+                    tmem_ld32(taddr + 32, s + 32);
+                    tmem_wait_ld();
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                    }
+                    const int gs = (g0 + h) % SCG;
+                    const float dxv = reinterpret_cast<const float*>(st)[row * SCG + gs];
+                    const uint64_t dx2 = pack2(dxv, dxv);
+                    const float* dwf = reinterpret_cast<const float*>(st + SC_DX + SC_DW) + gs * BN + cb;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 a = unpack2(acc[2 * i]), c = unpack2(acc[2 * i + 1]);
-                    *reinterpret_cast<float4*>(yr + 4 * i) = make_float4(a.x, a.y, c.x, c.y);
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 w = *reinterpret_cast<const float4*>(dwf + i * 4);
+                        fma2_scaled(acc[2 * i], s[4 * i], s[4 * i + 1], w.x, w.y, dx2);
+                        fma2_scaled(acc[2 * i + 1], s[4 * i + 2], s[4 * i + 3], w.z, w.w, dx2);
+                    }
                 }
-            } else {
+                if ((g0 + 1) % SCG == SCG - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
+                    ++sc;
+                }
+            }
+            if (!ok) break;
+            const Tile T = tile_at<kGrouped>(t, M, ga, n_tiles);
+            if (row < T.rows) {
+                int64_t orow;
+                if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
+                else orow = T.m0 + row;
+                float* yr = y + orow * ldy + T.n0 + cb;
+                const int64_t ncols = N - (T.n0 + cb);
+                if (vec4 && ncols >= 64) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 a = unpack2(acc[i]);
-                    if (2 * i < ncols) yr[2 * i] = a.x;
-                    if (2 * i + 1 < ncols) yr[2 * i + 1] = a.y;
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 a = unpack2(acc[2 * i]), c = unpack2(acc[2 * i + 1]);
+                        *reinterpret_cast<float4*>(yr + 4 * i) = make_float4(a.x, a.y, c.x, c.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 a = unpack2(acc[i]);
+                        if (2 * i < ncols) yr[2 * i] = a.x;
+                        if (2 * i + 1 < ncols) yr[2 * i + 1] = a.y;
+                    }
                 }
             }
         }
@@ -538,13 +577,14 @@ template <bool kQ4, bool kGrouped>
 cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& mb,
                           const CUtensorMap& mdx, const CUtensorMap& mdw, float* y, int64_t M,
                           int64_t N, int64_t K, int64_t ldy, GroupedArgs ga, int n_tiles,
-                          cudaStream_t s) {
+                          int64_t dense_tiles, cudaStream_t s) {
     cudaError_t e = ensure_smem_attr((const void*)tc_gemm_kernel<kQ4, kGrouped>, SMEM_BYTES,
                                      9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
     if (e != cudaSuccess) return e;
     const bool vec4 = ((uintptr_t)y % 16 == 0) && (ldy % 4 == 0);
     tc_gemm_kernel<kQ4, kGrouped><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
-                                                                    ldy, vec4, ga, n_tiles);
+                                                                    ldy, vec4, ga, n_tiles,
+                                                                    dense_tiles);
     return cudaGetLastError();
 }
 
@@ -577,10 +617,13 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dw, M, N, K, q4)) return cudaErrorInvalidValue;
-    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+    const int n_tiles = (int)((N + BN - 1) / BN);
+    const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
+    const int64_t ctas = tiles < sm_count() ? tiles : sm_count();
+    dim3 grid((unsigned)ctas);
     GroupedArgs ga{};
-    return q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, 0, s)
-              : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, 0, s);
+    return q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s)
+              : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s);
 }
 
 unsigned int read_and_clear_tc_error() {
