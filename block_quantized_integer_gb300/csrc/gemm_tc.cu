@@ -47,9 +47,9 @@ using namespace tc;
 
 constexpr int BM = 128, BN = 128;
 constexpr int GA = 2;                  // groups per A stage = one pair (64 binary16 = 128-byte rows)
-constexpr int NA = 5;                  // A stages
-constexpr int NB = 4;                  // B stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
-constexpr int NP = 2;                  // pair slots (binary16 B buffers and TMEM accumulators)
+constexpr int NO = 4;                  // operand slots: binary16 A stage + binary16 B pair
+constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
+constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int THREADS = 384;
@@ -66,11 +66,11 @@ constexpr int SC_DWF = SCG * BN * 4;                 // 4096: dw [8][128] f32
 constexpr int SC_STAGE = SC_DX + SC_DW + SC_DWF;     // 10240
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NA * A_STAGE;
+constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
-constexpr int OFF_SC = OFF_F16 + NP * F16_PAIR;
+constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 2 * NA + 2 * NB + 3 * NP + 3 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 3 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -80,19 +80,21 @@ constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of t
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;
 
+// full_a: TMA A stage landed; full_f16: converters wrote the B pair; ops_free:
+// the MMAs that read an operand slot completed (one commit frees A and B).
 struct Bars {
-    uint32_t full_a, empty_a, full_b, empty_b, full_f16, tfull, tempty, full_sc, ready_sc,
+    uint32_t full_a, full_f16, ops_free, full_b, empty_b, tfull, tempty, full_sc, ready_sc,
         empty_sc, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
     Bars b;
     b.full_a = base;
-    b.empty_a = b.full_a + 8 * NA;
-    b.full_b = b.empty_a + 8 * NA;
+    b.full_f16 = b.full_a + 8 * NO;
+    b.ops_free = b.full_f16 + 8 * NO;
+    b.full_b = b.ops_free + 8 * NO;
     b.empty_b = b.full_b + 8 * NB;
-    b.full_f16 = b.empty_b + 8 * NB;
-    b.tfull = b.full_f16 + 8 * NP;
+    b.tfull = b.empty_b + 8 * NB;
     b.tempty = b.tfull + 8 * NP;
     b.full_sc = b.tempty + 8 * NP;
     b.ready_sc = b.full_sc + 8 * NSC;
@@ -251,13 +253,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int64_t t0 = blockIdx.x, dt = gridDim.x;
 
     if (tid == 0) {
-        for (int i = 0; i < NA; ++i) { mbar_init(B.full_a + 8 * i, 1); mbar_init(B.empty_a + 8 * i, 1); }
+        for (int i = 0; i < NO; ++i) {
+            mbar_init(B.full_a + 8 * i, 1);
+            mbar_init(B.full_f16 + 8 * i, CONV_WARPS);
+            mbar_init(B.ops_free + 8 * i, 1);
+        }
         for (int i = 0; i < NB; ++i) {
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
         for (int i = 0; i < NP; ++i) {
-            mbar_init(B.full_f16 + 8 * i, CONV_WARPS);
             mbar_init(B.tfull + 8 * i, 1);
             mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
@@ -312,8 +317,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         ++ib;
                     }
                     if (g % GA == 0) {
-                        const int slot = (int)(ia % NA);
-                        if (!(ok = wait_bar<false>(B.empty_a + 8 * slot, ((ia / NA) & 1) ^ 1, abort))) break;
+                        const int slot = (int)(ia % NO);
+                        if (!(ok = wait_bar<false>(B.ops_free + 8 * slot, ((ia / NO) & 1) ^ 1, abort))) break;
                         mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
                         tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, g * 32, (int32_t)T.m0,
                                     B.full_a + 8 * slot);
@@ -322,8 +327,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 }
             }
             if (!ok) {
-                for (int64_t s = ia - NA; s < ia; ++s)
-                    if (s >= 0) drain_wait(B.full_a + 8 * (s % NA), (s / NA) & 1);
+                for (int64_t s = ia - NO; s < ia; ++s)
+                    if (s >= 0) drain_wait(B.full_a + 8 * (s % NO), (s / NO) & 1);
                 for (int64_t s = ib - NB; s < ib; ++s)
                     if (s >= 0) drain_wait(B.full_b + 8 * (s % NB), (s / NB) & 1);
                 for (int64_t s = isc - NSC; s < isc; ++s)
@@ -337,20 +342,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             int64_t p = 0;                                  // pair counter (A stage = pair)
             for (int64_t t = t0; t < num_tiles && ok; t += dt) {
                 for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                    const int sa = (int)(p % NA), ps = (int)(p % NP);
-                    const uint32_t pa = (uint32_t)((p / NA) & 1), pp = (uint32_t)((p / NP) & 1);
+                    const int so = (int)(p % NO), ps = (int)(p % NP);
+                    const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
                     // the three probes go out back to back; one branch on all of them
-                    const bool ready = mbar_try_wait(B.full_a + 8 * sa, pa) &
-                                       mbar_try_wait(B.full_f16 + 8 * ps, pp) &
+                    const bool ready = mbar_try_wait(B.full_a + 8 * so, po) &
+                                       mbar_try_wait(B.full_f16 + 8 * so, po) &
                                        mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
                     if (!ready) {
-                        if (!(ok = wait_bar<false>(B.full_a + 8 * sa, pa, abort))) break;
-                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * ps, pp, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
                         if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = sbase + OFF_A + sa * A_STAGE;
-                    const uint32_t b_s = sbase + OFF_F16 + ps * F16_PAIR;
+                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
+                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
                     const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
@@ -359,7 +364,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                             mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
                                     smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
                     mma_commit(B.tfull + 8 * ps);
-                    mma_commit(B.empty_a + 8 * sa);
+                    mma_commit(B.ops_free + 8 * so);
                     issued_any = true;
                 }
             }
@@ -391,17 +396,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     if (lane == 0) mbar_arrive(B.ready_sc + 8 * slot);
                     ++sc;
                 }
-                // the pair slot is free once the MMAs of pair p - NP completed
-                const int ps = (int)(p % NP);
-                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)(((p / NP) & 1) ^ 1), abort))) break;
+                // the operand slot is free once the MMAs of pair p - NO completed
+                const int so = (int)(p % NO);
+                if (!(ok = wait_bar<true>(B.ops_free + 8 * so, (uint32_t)(((p / NO) & 1) ^ 1), abort))) break;
                 const uint8_t* src = smem + OFF_B + (sb % NB) * B_STAGE;
-                uint8_t* dst = smem + OFF_F16 + ps * F16_PAIR;
+                uint8_t* dst = smem + OFF_F16 + so * F16_PAIR;
                 convert_group<kQ4>(src, dst, g0 % GB, ct);
                 convert_group<kQ4>(src, dst + F16_B, (g0 + 1) % GB, ct);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(B.full_f16 + 8 * ps);
+                    mbar_arrive(B.full_f16 + 8 * so);
                     if ((g0 + 1) % GB == GB - 1) mbar_arrive(B.empty_b + 8 * (sb % NB));
                 }
                 if ((g0 + 1) % GB == GB - 1) ++sb;
