@@ -125,8 +125,8 @@ def _dense(name, qx, dx, qw, dw, y, algo, workspace, wdtype, kfac):
     if workspace is None:
         op = OP_QGEMM_Q8_0 if kfac == 1 else OP_QGEMM_Q4_0
         nbytes = workspace_size(op, M, N, K)
-        if algo == ALGO_TCGEN05:      # explicit tensor-core path: binary16 activation codes
-            nbytes = max(nbytes, (M * K * 2 + 15) // 16 * 16)
+        if algo == ALGO_TCGEN05:      # explicit tensor-core path at any M
+            nbytes = max(nbytes, workspace_size(op, max(M, 9), N, K))
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0

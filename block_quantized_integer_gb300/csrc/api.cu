@@ -96,7 +96,7 @@ qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t
             return from_cuda(qg::launch_mma_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
         case QG_ALGO_TCGEN05:
             if (!qg::tc_gemm_supported(M, N, K, dx, dw)) return QG_ERR_UNSUPPORTED;
-            if (!ws || ws_bytes < qg::tc_gemm_workspace(M, K) || !aligned16(ws))
+            if (!ws || ws_bytes < qg::tc_gemm_workspace(M, N, K) || !aligned16(ws))
                 return QG_ERR_WORKSPACE;
             return from_cuda(qg::launch_tc_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, ws, s));
         default:
@@ -133,7 +133,7 @@ size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, 
     }
     if (op == QG_OP_QGEMM_Q8_0 || op == QG_OP_QGEMM_Q4_0) {
         // the tensor-core path widens the activation codes to binary16 first
-        if (M > 8 && K > 0 && K % 256 == 0) return qg::tc_gemm_workspace(M, K);
+        if (M > 8 && K > 0 && K % 256 == 0) return qg::tc_gemm_workspace(M, N, K);
         return 0;
     }
     return 0;

@@ -52,25 +52,25 @@ constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q
 constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
-constexpr int THREADS = 384;
-constexpr int EPI_WARPS = 8;
-constexpr int CONV_WARP0 = 10, CONV_WARPS = 2, CONV_THREADS = CONV_WARPS * 32;
+constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
+constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 2;
+constexpr int CONV_THREADS = CONV_WARPS * 32;
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 640
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
 constexpr int F16_B = BN * 32 * 2;                   // 8192: one group of binary16 B
 constexpr int F16_PAIR = 2 * F16_B;                  // 16384
 constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128][8] f32
-constexpr int SC_DW = BN * SCG * 2;                  // 2048: dw [128][8] f16
-constexpr int SC_DWF = SCG * BN * 4;                 // 4096: dw [8][128] f32
-constexpr int SC_STAGE = SC_DX + SC_DW + SC_DWF;     // 10240
+constexpr int SC_DW = SCG * BN * 4;                  // 4096: dw [8][128] f32 (transposed)
+constexpr int SC_STAGE = SC_DX + SC_DW;              // 8192
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
 constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 3 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 2 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -83,8 +83,7 @@ constexpr uint32_t kSpinLimit = 1u << 22;
 // full_a: TMA A stage landed; full_f16: converters wrote the B pair; ops_free:
 // the MMAs that read an operand slot completed (one commit frees A and B).
 struct Bars {
-    uint32_t full_a, full_f16, ops_free, full_b, empty_b, tfull, tempty, full_sc, ready_sc,
-        empty_sc, drain;
+    uint32_t full_a, full_f16, ops_free, full_b, empty_b, tfull, tempty, full_sc, empty_sc, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
@@ -97,8 +96,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     b.tfull = b.empty_b + 8 * NB;
     b.tempty = b.tfull + 8 * NP;
     b.full_sc = b.tempty + 8 * NP;
-    b.ready_sc = b.full_sc + 8 * NSC;
-    b.empty_sc = b.ready_sc + 8 * NSC;
+    b.empty_sc = b.full_sc + 8 * NSC;
     b.drain = b.empty_sc + 8 * NSC;
     return b;
 }
@@ -160,7 +158,7 @@ __device__ __forceinline__ uint32_t u4x2_to_h2(uint32_t nib_bytes, uint32_t sel)
 template <bool kQ4>
 __device__ __forceinline__ void convert_group(const uint8_t* src, uint8_t* dst, int gi, int ct) {
     if constexpr (!kQ4) {
-#pragma unroll
+#pragma unroll 2
         for (int j = 0; j < BN * 2 / CONV_THREADS; ++j) {
             const int i = ct + j * CONV_THREADS;
             const int row = i & (BN - 1), half = i >> 7;
@@ -174,26 +172,26 @@ __device__ __forceinline__ void convert_group(const uint8_t* src, uint8_t* dst, 
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < BN / CONV_THREADS; ++j) {
-            const int row = ct + j * CONV_THREADS;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((gi ^ (row & 7)) << 4));
-            // byte j: element j (low nibble), element j+16 (high nibble)
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t lo_h[8], hi_h[8];
+      for (int j = 0; j < BN / CONV_THREADS; ++j) {
+        const int row = ct + j * CONV_THREADS;        // one 16-byte group per row
+        const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((gi ^ (row & 7)) << 4));
+        // byte j: element j (low nibble), element j+16 (high nibble)
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t lo_h[8], hi_h[8];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
-                lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
-                lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
-                hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
-                hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
-            }
-            uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
-            *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
-            *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
-            *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
-            *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+            lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+            lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+            hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+            hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
         }
+        uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
+        *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+        *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+        *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+        *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+      }
     }
 }
 
@@ -207,10 +205,12 @@ struct GroupedArgs {
 
 struct Tile {
     int64_t m0, rows, n0, bn0;    // first A row, valid rows, first column, first B row
+    int64_t sg0;                  // first row of the transposed scale plane (expert * G)
 };
 
 template <bool kGrouped>
-__device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, const GroupedArgs& ga, int n_tiles) {
+__device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, int G, const GroupedArgs& ga,
+                                        int n_tiles) {
     Tile T;
     const int64_t mt = t / n_tiles;
     T.n0 = (t % n_tiles) * BN;
@@ -223,10 +223,12 @@ __device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, const GroupedArgs&
         T.m0 = ga.offsets[lo] + (mt - ga.tile_offsets[lo]) * BM;
         T.rows = min64(BM, (int64_t)ga.offsets[lo + 1] - T.m0);
         T.bn0 = (int64_t)lo * ga.N + T.n0;
+        T.sg0 = (int64_t)lo * G;
     } else {
         T.m0 = mt * BM;
         T.rows = min64(BM, M - T.m0);
         T.bn0 = T.n0;
+        T.sg0 = 0;
     }
     return T;
 }
@@ -249,8 +251,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int G = (int)(K / kGroup);                    // multiple of 8
     const int PAIRS = G / 2;
     constexpr int GB = kQ4 ? 8 : 4;                      // groups per B stage
-    const int64_t num_tiles = kGrouped ? (int64_t)ga.tile_offsets[ga.E] * n_tiles : dense_tiles;
-    const int64_t t0 = blockIdx.x, dt = gridDim.x;
+    const int num_tiles = kGrouped ? ga.tile_offsets[ga.E] * n_tiles : (int)dense_tiles;
+    const int t0 = blockIdx.x, dt = gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < NO; ++i) {
@@ -268,7 +270,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
         for (int i = 0; i < NSC; ++i) {
             mbar_init(B.full_sc + 8 * i, 1);
-            mbar_init(B.ready_sc + 8 * i, CONV_WARPS);
             mbar_init(B.empty_sc + 8 * i, EPI_WARPS);
         }
         mbar_init(B.drain, 1);
@@ -279,7 +280,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == PROD_WARP && lane == 0) {
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
         tma_prefetch_desc(&map_dx);
@@ -290,22 +291,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == PROD_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int64_t ia = 0, ib = 0, isc = 0;      // stages issued so far (run on across tiles)
             bool ok = true;
-            for (int64_t t = t0; t < num_tiles && ok; t += dt) {
-                const Tile T = tile_at<kGrouped>(t, M, ga, n_tiles);
+            for (int t = t0; t < num_tiles && ok; t += dt) {
+                const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
                 // issue in the order the stages are first needed
                 for (int g = 0; g < G && ok; ++g) {
                     if (g % SCG == 0) {
                         const int slot = (int)(isc % NSC);
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
                         const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
-                        mbar_expect_tx(B.full_sc + 8 * slot, SC_DX + SC_DW);
+                        mbar_expect_tx(B.full_sc + 8 * slot, SC_STAGE);
                         tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
-                        tma_load_2d(dst + SC_DX, &map_dw, g, (int32_t)T.bn0, B.full_sc + 8 * slot);
+                        tma_load_2d(dst + SC_DX, &map_dw, (int32_t)T.n0, (int32_t)(T.sg0 + g),
+                                    B.full_sc + 8 * slot);
                         ++isc;
                     }
                     if (g % GB == 0) {
@@ -335,12 +337,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     if (s >= 0) drain_wait(B.full_sc + 8 * (s % NSC), (s / NSC) & 1);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool issued_any = false, ok = true;
-            int64_t p = 0;                                  // pair counter (A stage = pair)
-            for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+            uint32_t p = 0;                                 // pair counter (A stage = pair)
+            for (int t = t0; t < num_tiles && ok; t += dt) {
                 for (int pl = 0; pl < PAIRS; ++pl, ++p) {
                     const int so = (int)(p % NO), ps = (int)(p % NP);
                     const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
@@ -376,26 +378,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     } else if (warp >= CONV_WARP0) {
         // ------------------------------------------------------------ converters
         const int ct = tid - CONV_WARP0 * 32;
-        int64_t p = 0, sb = 0, sc = 0;                      // run on across tiles
+        uint32_t p = 0, sb = 0;                             // run on across tiles
         bool ok = true;
-        for (int64_t t = t0; t < num_tiles && ok; t += dt) {
+        for (int t = t0; t < num_tiles && ok; t += dt) {
             for (int pl = 0; pl < PAIRS && ok; ++pl, ++p) {
                 const int g0 = 2 * pl;
                 if (g0 % GB == 0 && !(ok = wait_bar<true>(B.full_b + 8 * (sb % NB), (sb / NB) & 1, abort))) break;
-                if (g0 % SCG == 0) {
-                    const int slot = (int)(sc % NSC);
-                    if (!(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
-                    uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                    const uint16_t* dw_raw = reinterpret_cast<const uint16_t*>(st + SC_DX);
-                    float* dwf = reinterpret_cast<float*>(st + SC_DX + SC_DW);
-                    for (int idx = ct; idx < SCG * BN; idx += CONV_THREADS) {
-                        const int gg = idx >> 7, col = idx & (BN - 1);
-                        dwf[gg * BN + col] = half_bits_to_float(dw_raw[col * SCG + gg]);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B.ready_sc + 8 * slot);
-                    ++sc;
-                }
                 // the operand slot is free once the MMAs of pair p - NO completed
                 const int so = (int)(p % NO);
                 if (!(ok = wait_bar<true>(B.ops_free + 8 * so, (uint32_t)(((p / NO) & 1) ^ 1), abort))) break;
@@ -414,44 +402,46 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int wg = warp >> 2, q = warp & 3;
+        const int q = warp & 3;                             // TMEM lane quarter
         const int row = q * 32 + lane;
-        const int cb = wg * 64;
+        const int cb = (warp >> 2) * 32;                    // 32 columns per warp
         uint32_t p = 0, sc = 0;
         bool ok = true;
-        for (int64_t t = t0; t < num_tiles && ok; t += dt) {
-            uint64_t acc[32];
+        for (int t = t0; t < num_tiles && ok; t += dt) {
+            uint64_t acc[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0ull;
+            for (int i = 0; i < 16; ++i) acc[i] = 0ull;
             for (int pl = 0; pl < PAIRS; ++pl, ++p) {
                 const int g0 = 2 * pl, ps = (int)(p % NP);
                 const int slot = (int)(sc % NSC);
-                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.ready_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
                 if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)((p / NP) & 1), abort))) break;
                 tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * BN + cb);
                 const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+                const float* dxr = reinterpret_cast<const float*>(st) + row * SCG + (g0 % SCG);
+                const float2 dxv = *reinterpret_cast<const float2*>(dxr);
+                const float* dw0 = reinterpret_cast<const float*>(st + SC_DX) + (g0 % SCG) * BN + cb;
+                // the two groups of the pair one after the other (32 partials live);
+                // the other warps on this SMSP cover the TMEM latency
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)(ps * 2 * BN + h * BN + cb);
-                    uint32_t s[64];
-                    tmem_ld32(taddr, s);
-                    tmem_ld32(taddr + 32, s + 32);
+                    uint32_t sv[32];
+                    tmem_ld32(taddr + h * BN, sv);
                     tmem_wait_ld();
                     if (h == 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
                     }
-                    const int gs = (g0 + h) % SCG;
-                    const float dxv = reinterpret_cast<const float*>(st)[row * SCG + gs];
-                    const uint64_t dx2 = pack2(dxv, dxv);
-                    const float* dwf = reinterpret_cast<const float*>(st + SC_DX + SC_DW) + gs * BN + cb;
+                    const float dh = h ? dxv.y : dxv.x;
+                    const uint64_t d2 = pack2(dh, dh);
+                    const float* dwh = dw0 + h * BN;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float4 w = *reinterpret_cast<const float4*>(dwf + i * 4);
-                        fma2_scaled(acc[2 * i], s[4 * i], s[4 * i + 1], w.x, w.y, dx2);
-                        fma2_scaled(acc[2 * i + 1], s[4 * i + 2], s[4 * i + 3], w.z, w.w, dx2);
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
+                        fma2_scaled(acc[2 * i], sv[4 * i], sv[4 * i + 1], w.x, w.y, d2);
+                        fma2_scaled(acc[2 * i + 1], sv[4 * i + 2], sv[4 * i + 3], w.z, w.w, d2);
                     }
                 }
                 if ((g0 + 1) % SCG == SCG - 1) {
@@ -461,22 +451,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 }
             }
             if (!ok) break;
-            const Tile T = tile_at<kGrouped>(t, M, ga, n_tiles);
+            const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
             if (row < T.rows) {
                 int64_t orow;
                 if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
                 else orow = T.m0 + row;
                 float* yr = y + orow * ldy + T.n0 + cb;
                 const int64_t ncols = N - (T.n0 + cb);
-                if (vec4 && ncols >= 64) {
+                if (vec4 && ncols >= 32) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         const float2 a = unpack2(acc[2 * i]), c = unpack2(acc[2 * i + 1]);
                         *reinterpret_cast<float4*>(yr + 4 * i) = make_float4(a.x, a.y, c.x, c.y);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         const float2 a = unpack2(acc[i]);
                         if (2 * i < ncols) yr[2 * i] = a.x;
                         if (2 * i + 1 < ncols) yr[2 * i + 1] = a.y;
@@ -525,6 +515,21 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
     }
 }
 
+// dwT[r][n] = float(dw[n][g]) with r = e * G + g: the scale plane transposed to
+// group-major binary32 rows of ldt columns, the layout the epilogue reads.
+__global__ void __launch_bounds__(256)
+transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t G, int64_t E,
+                        float* __restrict__ dwt, int64_t ldt) {
+    const int64_t total = E * rows_n * G;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        // i walks dwT in order: e, g, n (coalesced writes)
+        const int64_t n = i % rows_n, eg = i / rows_n;
+        const int64_t g = eg % G, e = eg / G;
+        dwt[eg * ldt + n] = half_bits_to_float(dw[(e * rows_n + n) * G + g]);
+    }
+}
+
 // ---- host side ----------------------------------------------------------------------
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -562,10 +567,11 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 // Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
-// dx [rows][G], dw [brows][G].
+// dx [rows][G], transposed scales dwT [E*G][ldt] (binary32, n columns used).
 bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
-               const void* a16, const void* qw, const float* dx, const uint16_t* dw,
-               int64_t rows, int64_t brows, int64_t K, bool q4) {
+               const void* a16, const void* qw, const float* dx, const float* dwt,
+               int64_t rows, int64_t brows, int64_t n, int64_t ldt, int64_t sgrows, int64_t K,
+               bool q4) {
     const int64_t G = K / kGroup;
     const int64_t wbytes = q4 ? K / 2 : K;
     return make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
@@ -574,7 +580,7 @@ bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* 
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
                     CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_UINT16, dw, G, brows, G * 2, SCG, BN,
+           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dwt, n, sgrows, ldt * 4, BN, SCG,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -610,18 +616,26 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const vo
            encoder() != nullptr;
 }
 
-size_t tc_gemm_workspace(int64_t M, int64_t K) { return align16((size_t)M * K * 2); }
+int64_t ldt_of(int64_t N) { return (N + 3) / 4 * 4; }
+
+size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
+    return align16((size_t)M * K * 2) + align16((size_t)(K / kGroup) * ldt_of(N) * 4);
+}
 
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s) {
+    const int64_t G = K / kGroup, ldt = ldt_of(N);
     __half* a16 = static_cast<__half*>(workspace);
+    float* dwt = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16((size_t)M * K * 2));
     widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
                                                                nullptr, 1, 0);
+    transpose_scales_kernel<<<widen_grid(N * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dw, M, N, K, q4)) return cudaErrorInvalidValue;
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, N, ldt, G, K, q4))
+        return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
     const int64_t ctas = tiles < sm_count() ? tiles : sm_count();
