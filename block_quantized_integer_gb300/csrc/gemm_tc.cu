@@ -78,7 +78,9 @@ static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 
 
 constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of two groups
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
-constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
+constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
+constexpr uint32_t kSleepHintNs = 20000;             // a waiter sleeps until the phase flips
 
 // full_a: TMA A stage landed; full_f16: converters wrote the B pair; ops_free:
 // the MMAs that read an operand slot completed (one commit frees A and B).
@@ -101,22 +103,28 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     return b;
 }
 
-// Bounded wait.  kWarp: all 32 lanes call it and leave together.
+// Bounded wait: the thread sleeps in try_wait until the phase completes; after
+// kWaitCycles without completion (or when another role gave up) it returns
+// false.  kWarp: all 32 lanes call it and leave together.
 template <bool kWarp>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
-    for (uint32_t it = 1;; ++it) {
-        bool ok = mbar_try_wait(bar, parity);
+    bool ok = mbar_try_wait(bar, parity);
+    if (kWarp) ok = __all_sync(0xffffffffu, ok);
+    if (ok) return true;
+    const long long start = clock64();
+    for (;;) {
+        ok = mbar_try_wait_sleep(bar, parity, kSleepHintNs);
         if (kWarp) ok = __all_sync(0xffffffffu, ok);
         if (ok) return true;
-        if ((it & 63) == 0) {
-            bool ab = *abort != 0;
-            if (kWarp) ab = __any_sync(0xffffffffu, ab);
-            if (ab) return false;
-            if (it > kSpinLimit) {
-                *abort = 1;
-                atomicOr(&g_tc_error, 1u);
-                return false;
-            }
+        bool ab = *abort != 0;
+        if (kWarp) ab = __any_sync(0xffffffffu, ab);
+        if (ab) return false;
+        bool late = clock64() - start > kWaitCycles;
+        if (kWarp) late = __any_sync(0xffffffffu, late);
+        if (late) {
+            *abort = 1;
+            atomicOr(&g_tc_error, 1u);
+            return false;
         }
     }
 }
@@ -408,9 +416,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         uint32_t p = 0, sc = 0;
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
-            uint64_t acc[16];
+            float acc[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0ull;
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
             for (int pl = 0; pl < PAIRS; ++pl, ++p) {
                 const int g0 = 2 * pl, ps = (int)(p % NP);
                 const int slot = (int)(sc % NSC);
@@ -435,13 +443,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
                     }
                     const float dh = h ? dxv.y : dxv.x;
-                    const uint64_t d2 = pack2(dh, dh);
                     const float* dwh = dw0 + h * BN;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
-                        fma2_scaled(acc[2 * i], sv[4 * i], sv[4 * i + 1], w.x, w.y, d2);
-                        fma2_scaled(acc[2 * i + 1], sv[4 * i + 2], sv[4 * i + 3], w.z, w.w, d2);
+                        acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
+                        acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
+                        acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
+                        acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
                     }
                 }
                 if ((g0 + 1) % SCG == SCG - 1) {
@@ -460,17 +469,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 const int64_t ncols = N - (T.n0 + cb);
                 if (vec4 && ncols >= 32) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float2 a = unpack2(acc[2 * i]), c = unpack2(acc[2 * i + 1]);
-                        *reinterpret_cast<float4*>(yr + 4 * i) = make_float4(a.x, a.y, c.x, c.y);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(yr + 4 * i) =
+                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 a = unpack2(acc[i]);
-                        if (2 * i < ncols) yr[2 * i] = a.x;
-                        if (2 * i + 1 < ncols) yr[2 * i + 1] = a.y;
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i < ncols) yr[i] = acc[i];
                 }
             }
         }
