@@ -124,12 +124,17 @@ int qg_device_sm_count(void) { return qg::sm_count(); }
 
 unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 
+// The grouped product runs on the tensor cores when K % 256 == 0 (TMA scale
+// boxes), else on the warp-MMA kernel.
+bool moe_use_tc(int64_t K) { return K > 0 && K % 256 == 0; }
+
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
                             int32_t E) {
-    (void)N;
     if (op == QG_OP_GROUPED_MOE) {
         if (T < 0 || topk <= 0 || E <= 0) return 0;
-        return moe_ws(T * topk, E).total;
+        size_t w = moe_ws(T * topk, E).total;
+        if (moe_use_tc(K) && N > 0) w += qg::tc_grouped_workspace(T * topk, N, K, E);
+        return w;
     }
     if (op == QG_OP_QGEMM_Q8_0 || op == QG_OP_QGEMM_Q4_0) {
         // the tensor-core path widens the activation codes to binary16 first
@@ -227,15 +232,21 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
         ((uintptr_t)dw & 1u))
         return QG_ERR_ALIGNMENT;
     const MoeWs w = moe_ws(P, E);
-    if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return QG_ERR_WORKSPACE;
+    const bool tc = moe_use_tc(K) && ((uintptr_t)dx % 16 == 0) && ((uintptr_t)dw % 16 == 0);
+    const size_t need = w.total + (tc ? qg::tc_grouped_workspace(P, N, K, E) : 0);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QG_ERR_WORKSPACE;
     uint8_t* ws = (uint8_t*)workspace;
     int32_t* counts = (int32_t*)(ws + w.counts);
     int32_t* offsets = (int32_t*)(ws + w.offsets);
     int32_t* tiles = (int32_t*)(ws + w.tiles);
     int32_t* perm = (int32_t*)(ws + w.perm);
-    cudaError_t e = qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, tiles,
-                                         qg::mma_tile_m(), y, N, d_err, stream);
+    const int bm = tc ? qg::tc_tile_m() : qg::mma_tile_m();
+    cudaError_t e = qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, tiles, bm,
+                                         y, N, d_err, stream);
     if (e != cudaSuccess) return QG_ERR_CUDA;
+    if (tc)
+        return from_cuda(qg::launch_tc_grouped(qx, dx, P, N, K, qw4, dw, y, E, topk, x_row_mode,
+                                               perm, offsets, tiles, ws + w.total, stream));
     qg::GatherArgs ga{perm, offsets, tiles, E, topk, x_row_mode};
     return from_cuda(qg::launch_mma_grouped(qx, dx, P, N, K, qw4, dw, y, ga, stream));
 }

@@ -615,6 +615,8 @@ size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
 }  // namespace
 
+int tc_tile_m() { return BM; }
+
 bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const void* dw) {
     (void)M; (void)N;
     return K % 256 == 0 && ((uintptr_t)dx % 16 == 0) && ((uintptr_t)dw % 16 == 0) &&
@@ -648,6 +650,41 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     GroupedArgs ga{};
     return q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s)
               : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s);
+}
+
+// MoE workspace after the routing tables: a16 [P][K] binary16, dxg [P][G]
+// binary32 (gathered activation rows and scales in expert order) and the
+// transposed scales dwT [E*G][ldt] binary32.
+size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E) {
+    const int64_t G = K / kGroup;
+    return align16((size_t)P * K * 2) + align16((size_t)P * G * 4) +
+           align16((size_t)E * G * ldt_of(N) * 4);
+}
+
+cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N, int64_t K,
+                              const uint8_t* qw4, const uint16_t* dw, float* y, int32_t E,
+                              int32_t topk, int32_t x_row_mode, const int32_t* perm,
+                              const int32_t* offsets, const int32_t* tile_offsets,
+                              void* workspace, cudaStream_t s) {
+    const int64_t G = K / kGroup, ldt = ldt_of(N);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    __half* a16 = reinterpret_cast<__half*>(ws);
+    float* dxg = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2));
+    float* dwt = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2) + align16((size_t)P * G * 4));
+    // gather + widen the routed rows (count read on the device: offsets[E])
+    widen_rows_kernel<<<widen_grid(P * (K / 16)), 256, 0, s>>>(qx, dx, P, K, a16, dxg, perm,
+                                                               offsets + E, topk, x_row_mode);
+    transpose_scales_kernel<<<widen_grid((int64_t)E * N * G), 256, 0, s>>>(dw, N, G, E, dwt, ldt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb, mdx, mdw;
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dwt, P, (int64_t)E * N, N, ldt,
+                   (int64_t)E * G, K, true))
+        return cudaErrorInvalidValue;
+    const int n_tiles = (int)((N + BN - 1) / BN);
+    GroupedArgs ga{perm, offsets, tile_offsets, E, N};
+    dim3 grid((unsigned)sm_count());
+    return launch_kernel<true, true>(grid, ma, mb, mdx, mdw, y, P, N, K, N, ga, n_tiles, 0, s);
 }
 
 unsigned int read_and_clear_tc_error() {

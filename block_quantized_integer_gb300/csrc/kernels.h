@@ -44,6 +44,13 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s);
 unsigned int read_and_clear_tc_error();
+int tc_tile_m();
+size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E);
+cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N, int64_t K,
+                              const uint8_t* qw4, const uint16_t* dw, float* y, int32_t E,
+                              int32_t topk, int32_t x_row_mode, const int32_t* perm,
+                              const int32_t* offsets, const int32_t* tile_offsets,
+                              void* workspace, cudaStream_t s);
 
 // Routing: counts/offsets/perm (+ m-tile offsets for tile height bm when
 // tile_offsets != nullptr; + zeroing of unrouted rows of y when y != nullptr).

@@ -262,12 +262,13 @@ def test_moe_route_invalid_ids():
     assert np.array_equal(to_np(p)[: offsets[6]], perm)
 
 
+@pytest.mark.parametrize("K", [128, 512])      # K % 256 == 0 takes the tensor-core kernel
 @pytest.mark.parametrize("mode", [0, 1])
-def test_grouped_moe_small(mode):
-    rng, qw4, dw, ids = _moe_small()
+def test_grouped_moe_small(mode, K):
+    rng, qw4, dw, ids = _moe_small(K=K)
     T, topk = ids.shape
     rows = T if mode == 0 else T * topk
-    x = rng.standard_normal((rows, 128)).astype(np.float32)
+    x = rng.standard_normal((rows, K)).astype(np.float32)
     qx, dx = oracle.quantize_act_q8(x)
     y_ref, mag, bad = oracle.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw)
     y, d_err = qg.grouped_qgemm_moe(to_dev(qx), to_dev(dx), to_dev(ids), mode, to_dev(qw4),
@@ -277,12 +278,13 @@ def test_grouped_moe_small(mode):
     assert_close(to_np(y), y_ref, mag)
 
 
-def test_grouped_moe_unrouted_rows_zero_and_counted():
-    rng, qw4, dw, ids = _moe_small()
+@pytest.mark.parametrize("K", [128, 256])
+def test_grouped_moe_unrouted_rows_zero_and_counted(K):
+    rng, qw4, dw, ids = _moe_small(K=K)
     ids = ids.copy()
     ids[4, 1] = 9          # == E: out of range
     ids[10, 0] = -2
-    x = rng.standard_normal((ids.shape[0], 128)).astype(np.float32)
+    x = rng.standard_normal((ids.shape[0], K)).astype(np.float32)
     qx, dx = oracle.quantize_act_q8(x)
     y_ref, mag, bad = oracle.grouped_qgemm_moe(qx, dx, ids, 0, qw4, dw)
     y0 = torch.full((ids.size, 96), 5.0, device=dev())
@@ -293,14 +295,15 @@ def test_grouped_moe_unrouted_rows_zero_and_counted():
     assert_close(to_np(y), y_ref, mag)
 
 
-def test_grouped_moe_single_expert_equals_dense_q4():
-    rng, qw4, dw, _ = _moe_small()
+@pytest.mark.parametrize("K,algo", [(128, qg.ALGO_MMA), (512, qg.ALGO_TCGEN05)])
+def test_grouped_moe_single_expert_equals_dense_q4(K, algo):
+    rng, qw4, dw, _ = _moe_small(K=K)
     T = 300
     ids = np.full((T, 1), 6, np.int32)
-    x = rng.standard_normal((T, 128)).astype(np.float32)
+    x = rng.standard_normal((T, K)).astype(np.float32)
     qx, dx = qg.quantize_act_q8(to_dev(x))
     y, _ = qg.grouped_qgemm_moe(qx, dx, to_dev(ids), 0, to_dev(qw4), to_dev(dw))
-    yd = qg.qgemm_q4_0(qx, dx, to_dev(qw4[6]), to_dev(dw[6]), algo=qg.ALGO_MMA)
+    yd = qg.qgemm_q4_0(qx, dx, to_dev(qw4[6]), to_dev(dw[6]), algo=algo)
     _sync()
     assert torch.equal(y, yd)
 
