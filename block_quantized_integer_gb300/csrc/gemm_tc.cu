@@ -410,75 +410,109 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Software-pipelined over 16-column chunks: the TMEM load of the next
+        // chunk is in flight while the current one is scaled and accumulated.
+        // The four chunks of a pair are (group h, chunk c) = (0,0) (0,1) (1,0)
+        // (1,1), alternating between two register buffers.
         const int q = warp & 3;                             // TMEM lane quarter
         const int row = q * 32 + lane;
         const int cb = (warp >> 2) * 32;                    // 32 columns per warp
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint32_t s0[16], s1[16];
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        auto chunk_addr = [&](uint32_t pp, int hh, int cc) -> uint32_t {
+            return tmem_base + lane_off + (uint32_t)((pp % NP) * 2 * BN + hh * BN + cb + cc * 16);
+        };
+        // acquire pair pp (plocal within its tile): scale stage every 8 groups, TMEM slot
+        auto acquire = [&](uint32_t pp, int plocal, uint32_t scc) -> bool {
+            if ((2 * plocal) % SCG == 0 &&
+                !wait_bar<true>(B.full_sc + 8 * (scc % NSC), (scc / NSC) & 1, abort))
+                return false;
+            if (!wait_bar<true>(B.tfull + 8 * (pp % NP), (pp / NP) & 1, abort)) return false;
+            tc_fence_after();
+            return true;
+        };
+        // y[row][cb + c*16 + i] += S * (dx * dw) for one 16-column chunk
+        auto scale_chunk = [&](const uint32_t (&sv)[16], const uint8_t* st, int gs, int cc) {
+            const float dh = reinterpret_cast<const float*>(st)[row * SCG + gs];
+            const float* dwh = reinterpret_cast<const float*>(st + SC_DX) + gs * BN + cb + cc * 16;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
+                const int o = cc * 16 + i * 4;
+                acc[o + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[o + 0]);
+                acc[o + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[o + 1]);
+                acc[o + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[o + 2]);
+                acc[o + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[o + 3]);
+            }
+        };
+        int t = t0, pl = 0;
         uint32_t p = 0, sc = 0;
-        bool ok = true;
-        for (int t = t0; t < num_tiles && ok; t += dt) {
-            float acc[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                const int g0 = 2 * pl, ps = (int)(p % NP);
-                const int slot = (int)(sc % NSC);
-                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
-                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)((p / NP) & 1), abort))) break;
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * BN + cb);
-                const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                const float* dxr = reinterpret_cast<const float*>(st) + row * SCG + (g0 % SCG);
-                const float2 dxv = *reinterpret_cast<const float2*>(dxr);
-                const float* dw0 = reinterpret_cast<const float*>(st + SC_DX) + (g0 % SCG) * BN + cb;
-                // the two groups of the pair one after the other (32 partials live);
-                // the other warps on this SMSP cover the TMEM latency
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sv[32];
-                    tmem_ld32(taddr + h * BN, sv);
-                    tmem_wait_ld();
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
-                    }
-                    const float dh = h ? dxv.y : dxv.x;
-                    const float* dwh = dw0 + h * BN;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
-                        acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
-                        acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
-                        acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
-                        acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
-                    }
-                }
-                if ((g0 + 1) % SCG == SCG - 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
-                    ++sc;
-                }
+        bool ok = t < num_tiles && acquire(0, 0, 0);
+        if (ok) tmem_ld16(chunk_addr(0, 0, 0), s0);
+        while (ok) {
+            const uint8_t* st = smem + OFF_SC + (int)(sc % NSC) * SC_STAGE;
+            const int gs0 = (2 * pl) % SCG;
+            // chunk (0,0) in s0
+            tmem_wait_ld();
+            tmem_ld16(chunk_addr(p, 0, 1), s1);
+            scale_chunk(s0, st, gs0, 0);
+            // chunk (0,1) in s1
+            tmem_wait_ld();
+            tmem_ld16(chunk_addr(p, 1, 0), s0);
+            scale_chunk(s1, st, gs0, 1);
+            // chunk (1,0) in s0
+            tmem_wait_ld();
+            tmem_ld16(chunk_addr(p, 1, 1), s1);
+            scale_chunk(s0, st, gs0 + 1, 0);
+            // chunk (1,1) in s1: the pair's TMEM slot is free once it has landed
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.tempty + 8 * (p % NP));
+            // advance to the next pair and start its first load
+            const int cur_t = t, cur_pl = pl;
+            const uint32_t cur_sc = sc;
+            ++p;
+            if (gs0 + 1 == SCG - 1) ++sc;
+            if (++pl == PAIRS) {
+                pl = 0;
+                t += dt;
             }
-            if (!ok) break;
-            const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
-            if (row < T.rows) {
-                int64_t orow;
-                if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
-                else orow = T.m0 + row;
-                float* yr = y + orow * ldy + T.n0 + cb;
-                const int64_t ncols = N - (T.n0 + cb);
-                if (vec4 && ncols >= 32) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<float4*>(yr + 4 * i) =
-                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < ncols) yr[i] = acc[i];
-                }
+            const bool more = t < num_tiles && (ok = acquire(p, pl, sc));
+            if (more) tmem_ld16(chunk_addr(p, 0, 0), s0);
+            scale_chunk(s1, st, gs0 + 1, 1);
+            if (gs0 + 1 == SCG - 1) {                      // last group of the scale stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B.empty_sc + 8 * (int)(cur_sc % NSC));
             }
+            if (cur_pl == PAIRS - 1) {                      // end of a tile: write y
+                const Tile T = tile_at<kGrouped>(cur_t, M, G, ga, n_tiles);
+                if (row < T.rows) {
+                    int64_t orow;
+                    if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
+                    else orow = T.m0 + row;
+                    float* yr = y + orow * ldy + T.n0 + cb;
+                    const int64_t ncols = N - (T.n0 + cb);
+                    if (vec4 && ncols >= 32) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<float4*>(yr + 4 * i) =
+                                make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < ncols) yr[i] = acc[i];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            }
+            if (!more) break;
         }
+        tmem_wait_ld();
     }
 
     tc_fence_before();
