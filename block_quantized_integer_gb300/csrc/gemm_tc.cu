@@ -49,7 +49,7 @@ constexpr int BM = 128, BN = 128;
 constexpr int GA = 2;                  // groups per A stage = one pair (64 binary16 = 128-byte rows)
 constexpr int NO = 4;                  // operand slots: binary16 A stage + binary16 B pair
 constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
-constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
+constexpr int NT = 4;                  // TMEM group slots (128 columns each)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
@@ -70,13 +70,13 @@ constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
 constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 2 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NT + 2 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 KiB alignment");
 
-constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of two groups
+constexpr uint32_t TMEM_COLS = NT * BN;              // 512: four group slots
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
 constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
@@ -96,8 +96,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     b.full_b = b.ops_free + 8 * NO;
     b.empty_b = b.full_b + 8 * NB;
     b.tfull = b.empty_b + 8 * NB;
-    b.tempty = b.tfull + 8 * NP;
-    b.full_sc = b.tempty + 8 * NP;
+    b.tempty = b.tfull + 8 * NT;
+    b.full_sc = b.tempty + 8 * NT;
     b.empty_sc = b.full_sc + 8 * NSC;
     b.drain = b.empty_sc + 8 * NSC;
     return b;
@@ -272,7 +272,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NP; ++i) {
+        for (int i = 0; i < NT; ++i) {
             mbar_init(B.tfull + 8 * i, 1);
             mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
@@ -347,34 +347,38 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
+        // Operands arrive per pair of groups (one A stage, one binary16 B
+        // pair); each group's two K=16 MMAs go to their own TMEM slot.
         if (lane == 0) {
             bool issued_any = false, ok = true;
-            uint32_t p = 0;                                 // pair counter (A stage = pair)
+            uint32_t g = 0;                                 // global group counter
             for (int t = t0; t < num_tiles && ok; t += dt) {
-                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                    const int so = (int)(p % NO), ps = (int)(p % NP);
-                    const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
-                    // the three probes go out back to back; one branch on all of them
-                    const bool ready = mbar_try_wait(B.full_a + 8 * so, po) &
-                                       mbar_try_wait(B.full_f16 + 8 * so, po) &
-                                       mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
+                for (int gl = 0; gl < G; ++gl, ++g) {
+                    const uint32_t pr = g >> 1;
+                    const int so = (int)(pr % NO), ts = (int)(g % NT), h = (int)(g & 1);
+                    const uint32_t po = (pr / NO) & 1, pt = ((g / NT) & 1) ^ 1;
+                    // the probes go out back to back; one branch on all of them
+                    bool ready = mbar_try_wait(B.tempty + 8 * ts, pt);
+                    if (h == 0)
+                        ready = ready & mbar_try_wait(B.full_a + 8 * so, po) &
+                                mbar_try_wait(B.full_f16 + 8 * so, po);
                     if (!ready) {
-                        if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
-                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
-                        if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
+                        if (h == 0) {
+                            if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
+                            if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
+                        }
+                        if (!(ok = wait_bar<false>(B.tempty + 8 * ts, pt, abort))) break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
-                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
-                    const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
+                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE + h * 64;
+                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR + h * F16_B;
+                    const uint32_t d = tmem_base + (uint32_t)(ts * BN);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-                            mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
-                                    smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
-                    mma_commit(B.tfull + 8 * ps);
-                    mma_commit(B.ops_free + 8 * so);
+                    for (int j = 0; j < 2; ++j)
+                        mma_f16(d, smem_desc_sw128(a_s + j * 32),
+                                smem_desc_noswizzle(b_s + j * 256, 128, 512), IDESC, j);
+                    mma_commit(B.tfull + 8 * ts);
+                    if (h == 1) mma_commit(B.ops_free + 8 * so);
                     issued_any = true;
                 }
             }
@@ -410,109 +414,67 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Software-pipelined over 16-column chunks: the TMEM load of the next
-        // chunk is in flight while the current one is scaled and accumulated.
-        // The four chunks of a pair are (group h, chunk c) = (0,0) (0,1) (1,0)
-        // (1,1), alternating between two register buffers.
+        // Per group: one TMEM load of the warp's 32 columns, the slot released
+        // as soon as it has landed, then y += S * (dx * dw) in registers.
         const int q = warp & 3;                             // TMEM lane quarter
         const int row = q * 32 + lane;
         const int cb = (warp >> 2) * 32;                    // 32 columns per warp
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint32_t s0[16], s1[16];
-        float acc[32];
+        uint32_t g = 0, sc = 0;
+        bool ok = true;
+        for (int t = t0; t < num_tiles && ok; t += dt) {
+            float acc[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-        auto chunk_addr = [&](uint32_t pp, int hh, int cc) -> uint32_t {
-            return tmem_base + lane_off + (uint32_t)((pp % NP) * 2 * BN + hh * BN + cb + cc * 16);
-        };
-        // acquire pair pp (plocal within its tile): scale stage every 8 groups, TMEM slot
-        auto acquire = [&](uint32_t pp, int plocal, uint32_t scc) -> bool {
-            if ((2 * plocal) % SCG == 0 &&
-                !wait_bar<true>(B.full_sc + 8 * (scc % NSC), (scc / NSC) & 1, abort))
-                return false;
-            if (!wait_bar<true>(B.tfull + 8 * (pp % NP), (pp / NP) & 1, abort)) return false;
-            tc_fence_after();
-            return true;
-        };
-        // y[row][cb + c*16 + i] += S * (dx * dw) for one 16-column chunk
-        auto scale_chunk = [&](const uint32_t (&sv)[16], const uint8_t* st, int gs, int cc) {
-            const float dh = reinterpret_cast<const float*>(st)[row * SCG + gs];
-            const float* dwh = reinterpret_cast<const float*>(st + SC_DX) + gs * BN + cb + cc * 16;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
-                const int o = cc * 16 + i * 4;
-                acc[o + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[o + 0]);
-                acc[o + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[o + 1]);
-                acc[o + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[o + 2]);
-                acc[o + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[o + 3]);
-            }
-        };
-        int t = t0, pl = 0;
-        uint32_t p = 0, sc = 0;
-        bool ok = t < num_tiles && acquire(0, 0, 0);
-        if (ok) tmem_ld16(chunk_addr(0, 0, 0), s0);
-        while (ok) {
-            const uint8_t* st = smem + OFF_SC + (int)(sc % NSC) * SC_STAGE;
-            const int gs0 = (2 * pl) % SCG;
-            // chunk (0,0) in s0
-            tmem_wait_ld();
-            tmem_ld16(chunk_addr(p, 0, 1), s1);
-            scale_chunk(s0, st, gs0, 0);
-            // chunk (0,1) in s1
-            tmem_wait_ld();
-            tmem_ld16(chunk_addr(p, 1, 0), s0);
-            scale_chunk(s1, st, gs0, 1);
-            // chunk (1,0) in s0
-            tmem_wait_ld();
-            tmem_ld16(chunk_addr(p, 1, 1), s1);
-            scale_chunk(s0, st, gs0 + 1, 0);
-            // chunk (1,1) in s1: the pair's TMEM slot is free once it has landed
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.tempty + 8 * (p % NP));
-            // advance to the next pair and start its first load
-            const int cur_t = t, cur_pl = pl;
-            const uint32_t cur_sc = sc;
-            ++p;
-            if (gs0 + 1 == SCG - 1) ++sc;
-            if (++pl == PAIRS) {
-                pl = 0;
-                t += dt;
-            }
-            const bool more = t < num_tiles && (ok = acquire(p, pl, sc));
-            if (more) tmem_ld16(chunk_addr(p, 0, 0), s0);
-            scale_chunk(s1, st, gs0 + 1, 1);
-            if (gs0 + 1 == SCG - 1) {                      // last group of the scale stage
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int gl = 0; gl < G; ++gl, ++g) {
+                const int ts = (int)(g % NT), slot = (int)(sc % NSC);
+                if (gl % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                if (!(ok = wait_bar<true>(B.tfull + 8 * ts, (g / NT) & 1, abort))) break;
+                tc_fence_after();
+                uint32_t sv[32];
+                tmem_ld32(tmem_base + lane_off + (uint32_t)(ts * BN + cb), sv);
+                tmem_wait_ld();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(B.empty_sc + 8 * (int)(cur_sc % NSC));
-            }
-            if (cur_pl == PAIRS - 1) {                      // end of a tile: write y
-                const Tile T = tile_at<kGrouped>(cur_t, M, G, ga, n_tiles);
-                if (row < T.rows) {
-                    int64_t orow;
-                    if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
-                    else orow = T.m0 + row;
-                    float* yr = y + orow * ldy + T.n0 + cb;
-                    const int64_t ncols = N - (T.n0 + cb);
-                    if (vec4 && ncols >= 32) {
+                if (lane == 0) mbar_arrive(B.tempty + 8 * ts);
+                const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
+                const int gs = gl % SCG;
+                const float dh = reinterpret_cast<const float*>(st)[row * SCG + gs];
+                const float* dwh = reinterpret_cast<const float*>(st + SC_DX) + gs * BN + cb;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<float4*>(yr + 4 * i) =
-                                make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < ncols) yr[i] = acc[i];
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
+                    acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
+                    acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
                 }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                if (gs == SCG - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
+                    ++sc;
+                }
             }
-            if (!more) break;
+            if (!ok) break;
+            const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
+            if (row < T.rows) {
+                int64_t orow;
+                if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
+                else orow = T.m0 + row;
+                float* yr = y + orow * ldy + T.n0 + cb;
+                const int64_t ncols = N - (T.n0 + cb);
+                if (vec4 && ncols >= 32) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(yr + 4 * i) =
+                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < ncols) yr[i] = acc[i];
+                }
+            }
         }
-        tmem_wait_ld();
     }
 
     tc_fence_before();
