@@ -49,7 +49,7 @@ constexpr int BM = 128, BN = 128;
 constexpr int GA = 2;                  // groups per A stage = one pair (64 binary16 = 128-byte rows)
 constexpr int NO = 4;                  // operand slots: binary16 A stage + binary16 B pair
 constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
-constexpr int NT = 4;                  // TMEM group slots (128 columns each)
+constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
@@ -70,13 +70,13 @@ constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
 constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NT + 2 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 2 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 KiB alignment");
 
-constexpr uint32_t TMEM_COLS = NT * BN;              // 512: four group slots
+constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of two groups
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
 constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
@@ -96,8 +96,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     b.full_b = b.ops_free + 8 * NO;
     b.empty_b = b.full_b + 8 * NB;
     b.tfull = b.empty_b + 8 * NB;
-    b.tempty = b.tfull + 8 * NT;
-    b.full_sc = b.tempty + 8 * NT;
+    b.tempty = b.tfull + 8 * NP;
+    b.full_sc = b.tempty + 8 * NP;
     b.empty_sc = b.full_sc + 8 * NSC;
     b.drain = b.empty_sc + 8 * NSC;
     return b;
@@ -272,7 +272,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NT; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(B.tfull + 8 * i, 1);
             mbar_init(B.tempty + 8 * i, EPI_WARPS);
         }
@@ -347,38 +347,34 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        // Operands arrive per pair of groups (one A stage, one binary16 B
-        // pair); each group's two K=16 MMAs go to their own TMEM slot.
         if (lane == 0) {
             bool issued_any = false, ok = true;
-            uint32_t g = 0;                                 // global group counter
+            uint32_t p = 0;                                 // pair counter (A stage = pair)
             for (int t = t0; t < num_tiles && ok; t += dt) {
-                for (int gl = 0; gl < G; ++gl, ++g) {
-                    const uint32_t pr = g >> 1;
-                    const int so = (int)(pr % NO), ts = (int)(g % NT), h = (int)(g & 1);
-                    const uint32_t po = (pr / NO) & 1, pt = ((g / NT) & 1) ^ 1;
-                    // the probes go out back to back; one branch on all of them
-                    bool ready = mbar_try_wait(B.tempty + 8 * ts, pt);
-                    if (h == 0)
-                        ready = ready & mbar_try_wait(B.full_a + 8 * so, po) &
-                                mbar_try_wait(B.full_f16 + 8 * so, po);
+                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                    const int so = (int)(p % NO), ps = (int)(p % NP);
+                    const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
+                    // the three probes go out back to back; one branch on all of them
+                    const bool ready = mbar_try_wait(B.full_a + 8 * so, po) &
+                                       mbar_try_wait(B.full_f16 + 8 * so, po) &
+                                       mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
                     if (!ready) {
-                        if (h == 0) {
-                            if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
-                            if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
-                        }
-                        if (!(ok = wait_bar<false>(B.tempty + 8 * ts, pt, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
+                        if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE + h * 64;
-                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR + h * F16_B;
-                    const uint32_t d = tmem_base + (uint32_t)(ts * BN);
+                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
+                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
+                    const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        mma_f16(d, smem_desc_sw128(a_s + j * 32),
-                                smem_desc_noswizzle(b_s + j * 256, 128, 512), IDESC, j);
-                    mma_commit(B.tfull + 8 * ts);
-                    if (h == 1) mma_commit(B.ops_free + 8 * so);
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
+                                    smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
+                    mma_commit(B.tfull + 8 * ps);
+                    mma_commit(B.ops_free + 8 * so);
                     issued_any = true;
                 }
             }
@@ -414,42 +410,50 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Per group: one TMEM load of the warp's 32 columns, the slot released
-        // as soon as it has landed, then y += S * (dx * dw) in registers.
         const int q = warp & 3;                             // TMEM lane quarter
         const int row = q * 32 + lane;
         const int cb = (warp >> 2) * 32;                    // 32 columns per warp
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint32_t g = 0, sc = 0;
+        uint32_t p = 0, sc = 0;
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int gl = 0; gl < G; ++gl, ++g) {
-                const int ts = (int)(g % NT), slot = (int)(sc % NSC);
-                if (gl % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
-                if (!(ok = wait_bar<true>(B.tfull + 8 * ts, (g / NT) & 1, abort))) break;
+            for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                const int g0 = 2 * pl, ps = (int)(p % NP);
+                const int slot = (int)(sc % NSC);
+                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)((p / NP) & 1), abort))) break;
                 tc_fence_after();
-                uint32_t sv[32];
-                tmem_ld32(tmem_base + lane_off + (uint32_t)(ts * BN + cb), sv);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.tempty + 8 * ts);
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * BN + cb);
                 const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                const int gs = gl % SCG;
-                const float dh = reinterpret_cast<const float*>(st)[row * SCG + gs];
-                const float* dwh = reinterpret_cast<const float*>(st + SC_DX) + gs * BN + cb;
+                const float* dxr = reinterpret_cast<const float*>(st) + row * SCG + (g0 % SCG);
+                const float2 dxv = *reinterpret_cast<const float2*>(dxr);
+                const float* dw0 = reinterpret_cast<const float*>(st + SC_DX) + (g0 % SCG) * BN + cb;
+                // the two groups of the pair one after the other (32 partials live);
+                // the other warps on this SMSP cover the TMEM latency
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sv[32];
+                    tmem_ld32(taddr + h * BN, sv);
+                    tmem_wait_ld();
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                    }
+                    const float dh = h ? dxv.y : dxv.x;
+                    const float* dwh = dw0 + h * BN;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
-                    acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
-                    acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
-                    acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
-                    acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
+                        acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
+                        acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
+                        acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
+                        acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
+                    }
                 }
-                if (gs == SCG - 1) {
+                if ((g0 + 1) % SCG == SCG - 1) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
                     ++sc;
