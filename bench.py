@@ -167,6 +167,62 @@ def make_decode(dev, M, seed_sub=0):
     return projs
 
 
+class DecodeGraphs:
+    """The decode step captured in CUDA graphs (the launch sequence is fixed,
+    so graph replay removes per-launch host overhead from the small GEMVs):
+    graph `head` = the four activation quantizations + the three small GEMVs,
+    graph `lm` = the lm-head GEMV alone (timed on its own with events);
+    graph `e2e` = host copies in, the whole step, host copies out."""
+
+    def __init__(self, projs):
+        import torch
+        import block_quantized_integer_gb300 as qg
+        self.projs = projs
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(2):                      # warm up (allocations, attributes)
+                self._head(qg)
+                self._lm(qg)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.g_head, self.g_lm, self.g_e2e = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                              torch.cuda.CUDAGraph())
+        with torch.cuda.graph(self.g_head):
+            self._head(qg)
+        with torch.cuda.graph(self.g_lm):
+            self._lm(qg)
+        with torch.cuda.graph(self.g_e2e):
+            for p in projs:
+                p["x"].copy_(p["x_host"], non_blocking=True)
+            self._head(qg)
+            self._lm(qg)
+            for p in projs:
+                p["y_host"].copy_(p["y"], non_blocking=True)
+        torch.cuda.synchronize()
+
+    def _head(self, qg):
+        for p in self.projs:
+            qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
+        for p in self.projs[:-1]:
+            qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+
+    def _lm(self, qg):
+        p = self.projs[-1]
+        qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+
+    def step(self, timer=None):
+        self.g_head.replay()
+        if timer is not None:
+            timer[0].record()
+        self.g_lm.replay()
+        if timer is not None:
+            timer[1].record()
+
+    def step_e2e(self, timer=None):
+        self.g_e2e.replay()
+
+
 def decode_step(projs, timer=None):
     import block_quantized_integer_gb300 as qg
     for j, p in enumerate(projs):
@@ -176,15 +232,6 @@ def decode_step(projs, timer=None):
         qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
         if timer is not None and j == len(projs) - 1:
             timer[1].record()
-
-
-def decode_step_e2e(projs):
-    import block_quantized_integer_gb300 as qg
-    for p in projs:
-        p["x"].copy_(p["x_host"], non_blocking=True)
-        qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
-        qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
-        p["y_host"].copy_(p["y"], non_blocking=True)
 
 
 def timed(fn, steps, warmup, dist=None, per_kernel=None):
@@ -328,8 +375,8 @@ def main():
             out = moe_section(dev, peaks, reps=args.reps)
         else:
             projs = make_decode(dev, 1)
-            ms, kms = timed(lambda tm: decode_step(projs, tm), args.steps, args.warmup, None,
-                            per_kernel=True)
+            graphs = DecodeGraphs(projs)
+            ms, kms = timed(graphs.step, args.steps, args.warmup, None, per_kernel=True)
             from block_quantized_integer_gb300 import inputs as _in
             out = {"gbs": decode_bytes(1, _in.DECODE_SHAPES) * args.steps / (ms * 1e-3) / 1e9,
                    "lm_head_ms": kms}
@@ -384,16 +431,16 @@ def main():
     peaks = load_peaks()
 
     projs = make_decode(dev, 1)
+    graphs = DecodeGraphs(projs)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ms, kms = timed(lambda tm: decode_step(projs, tm), args.steps, args.warmup, dist,
-                    per_kernel=True)
+    ms, kms = timed(graphs.step, args.steps, args.warmup, dist, per_kernel=True)
     clocks = sampler.stop()
     value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
 
     # end to end: pinned host x in, y out, every step
-    ms_e2e, _ = timed(lambda tm: decode_step_e2e(projs), max(args.steps // 4, 10), 3, dist)
+    ms_e2e, _ = timed(graphs.step_e2e, max(args.steps // 4, 10), 3, dist)
     e2e = world * bytes_step * max(args.steps // 4, 10) / (ms_e2e * 1e-3) / 1e9
     h2d = sum(p["x_host"].numel() * 4 for p in projs)
     d2h = sum(p["y_host"].numel() * 4 for p in projs)
@@ -417,18 +464,20 @@ def main():
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * len(projs) * args.steps,
+        "launch": "CUDA graphs (quantize x4 + three GEMVs; lm-head GEMV)",
         "clocks": clocks,
     }
-    del projs
+    del graphs, projs
     torch.cuda.empty_cache()
 
     if not args.no_extra and rank == 0:
         projs4 = make_decode(dev, 4)
-        ms4, _ = timed(lambda tm: decode_step(projs4), max(args.steps // 2, 10), 5)
+        g4 = DecodeGraphs(projs4)
+        ms4, _ = timed(g4.step, max(args.steps // 2, 10), 5)
         b4 = decode_bytes(4, shapes)
         line["decode_m4"] = {"gbs": b4 * max(args.steps // 2, 10) / (ms4 * 1e-3) / 1e9,
                              "ms_per_step": ms4 / max(args.steps // 2, 10)}
-        del projs4
+        del g4, projs4
         torch.cuda.empty_cache()
         line["prefill"] = prefill_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()

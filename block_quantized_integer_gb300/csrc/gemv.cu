@@ -30,12 +30,12 @@ namespace {
 constexpr int kWarps = 8;
 
 template <int M, int R, bool kQ4, int W>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 gemv_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
             const uint8_t* __restrict__ qw, const uint16_t* __restrict__ dw,
             float* __restrict__ y, int64_t N, int64_t K, int64_t ldy) {
     constexpr int SETS = kWarps / W;          // row sets per block
-    constexpr int U = (R >= 4) ? 2 : 4;       // steps in flight per lane
+    constexpr int U = (R >= 4) ? 1 : 4;       // steps in flight per lane (x R rows)
     __shared__ float part[kWarps][R][M];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = K / kGroup;
