@@ -43,6 +43,11 @@ def decode_bytes(M, shapes):
     return sum(N * K * (1 + 2 / 32) + M * K * (1 + 4 / 32) + M * N * 4 for N, K in shapes)
 
 
+# DRAM bytes (read + write) of one lm-head GEMV launch, from the ncu capture
+# summarised in profiles/gemv_q8_lmhead_151936x4096_m1.md (same kernel build).
+LM_HEAD_TRAFFIC_BYTES = 661.329408e6 + 3.080704e6
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -458,7 +463,8 @@ def main():
                                             "no flush"},
         "frac_of_hbm": value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": LM_HEAD_TRAFFIC_BYTES, "algorithmic_bytes": lm_bytes,
                      "kernel": "gemv_kernel (151936x4096 Q8_0, M=1)",
                      "peak_source": peaks["source"] + " STREAM-style copy"},
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
