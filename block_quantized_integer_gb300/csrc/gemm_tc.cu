@@ -61,7 +61,7 @@ constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
 constexpr int F16_B = BN * 32 * 2;                   // 8192: one group of binary16 B
 constexpr int F16_PAIR = 2 * F16_B;                  // 16384
-constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128][8] f32
+constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [8][128] f32 (dense) or [128][8] (grouped)
 constexpr int SC_DW = SCG * BN * 4;                  // 4096: dw [8][128] f32 (transposed)
 constexpr int SC_STAGE = SC_DX + SC_DW;              // 8192
 
@@ -313,7 +313,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
                         const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
                         mbar_expect_tx(B.full_sc + 8 * slot, SC_STAGE);
-                        tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
+                        // dense: dx transposed (x = first row, a multiple of 128);
+                        // grouped: dx row-major (segment starts are arbitrary rows)
+                        if constexpr (kGrouped)
+                            tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
+                        else
+                            tma_load_2d(dst, &map_dx, (int32_t)T.m0, g, B.full_sc + 8 * slot);
                         tma_load_2d(dst + SC_DX, &map_dw, (int32_t)T.n0, (int32_t)(T.sg0 + g),
                                     B.full_sc + 8 * slot);
                         ++isc;
@@ -427,8 +432,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * BN + cb);
                 const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                const float* dxr = reinterpret_cast<const float*>(st) + row * SCG + (g0 % SCG);
-                const float2 dxv = *reinterpret_cast<const float2*>(dxr);
+                float2 dxv;
+                if constexpr (kGrouped) {
+                    dxv = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(st) +
+                                                           row * SCG + (g0 % SCG));
+                } else {                                    // contiguous over the warp's rows
+                    const float* dxt = reinterpret_cast<const float*>(st) + (g0 % SCG) * BM + row;
+                    dxv = make_float2(dxt[0], dxt[BM]);
+                }
                 const float* dw0 = reinterpret_cast<const float*>(st + SC_DX) + (g0 % SCG) * BN + cb;
                 // the two groups of the pair one after the other (32 partials live);
                 // the other warps on this SMSP cover the TMEM latency
@@ -535,6 +546,19 @@ transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t
     }
 }
 
+// dxt[g][m] = dx[m][g]: activation scales transposed to group-major rows of
+// ldm columns, so the epilogue's 32 rows of one group are contiguous.
+__global__ void __launch_bounds__(256)
+transpose_dx_kernel(const float* __restrict__ dx, int64_t M, int64_t G, float* __restrict__ dxt,
+                    int64_t ldm) {
+    const int64_t total = M * G;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i % M, g = i / M;               // writes coalesced along m
+        dxt[g * ldm + m] = dx[m * G + g];
+    }
+}
+
 // ---- host side ----------------------------------------------------------------------
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -573,18 +597,23 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 
 // Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
 // dx [rows][G], transposed scales dwT [E*G][ldt] (binary32, n columns used).
+// ldm > 0: dx is the transposed plane dxt [G][ldm]; ldm == 0: dx is [rows][G].
 bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
                const void* a16, const void* qw, const float* dx, const float* dwt,
                int64_t rows, int64_t brows, int64_t n, int64_t ldt, int64_t sgrows, int64_t K,
-               bool q4) {
+               bool q4, int64_t ldm) {
     const int64_t G = K / kGroup;
     const int64_t wbytes = q4 ? K / 2 : K;
+    const bool dx_ok = ldm > 0
+        ? make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, rows, G, ldm * 4, BM, SCG,
+                   CU_TENSOR_MAP_SWIZZLE_NONE)
+        : make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!dx_ok) return false;
     return make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
-                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
            make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dwt, n, sgrows, ldt * 4, BN, SCG,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -625,23 +654,29 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const vo
 
 int64_t ldt_of(int64_t N) { return (N + 3) / 4 * 4; }
 
+// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32 | dxT [G][ldt(M)] binary32
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
-    return align16((size_t)M * K * 2) + align16((size_t)(K / kGroup) * ldt_of(N) * 4);
+    const int64_t G = K / kGroup;
+    return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4) +
+           align16((size_t)G * ldt_of(M) * 4);
 }
 
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s) {
-    const int64_t G = K / kGroup, ldt = ldt_of(N);
-    __half* a16 = static_cast<__half*>(workspace);
-    float* dwt = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16((size_t)M * K * 2));
+    const int64_t G = K / kGroup, ldt = ldt_of(N), ldm = ldt_of(M);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    __half* a16 = reinterpret_cast<__half*>(ws);
+    float* dwt = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2));
+    float* dxt = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2) + align16((size_t)G * ldt * 4));
     widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
                                                                nullptr, 1, 0);
     transpose_scales_kernel<<<widen_grid(N * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
+    transpose_dx_kernel<<<widen_grid(M * G), 256, 0, s>>>(dx, M, G, dxt, ldm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, N, ldt, G, K, q4))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dxt, dwt, M, N, N, ldt, G, K, q4, ldm))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
@@ -679,7 +714,7 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dwt, P, (int64_t)E * N, N, ldt,
-                   (int64_t)E * G, K, true))
+                   (int64_t)E * G, K, true, 0))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     GroupedArgs ga{perm, offsets, tile_offsets, E, N};
