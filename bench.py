@@ -270,14 +270,17 @@ def timed(fn, steps, warmup, dist=None, per_kernel=None):
     return ms, kms
 
 
-def prefill_section(dev, peaks, reps=20):
-    """Prefill GEMM M=2048 (both shapes): int8-equivalent TOPS = 2MNK / t."""
+def prefill_section(dev, peaks, reps=20, long_ctx=False):
+    """Prefill GEMM M=2048 (both shapes), or the M=18432 long-context shapes:
+    int8-equivalent TOPS = 2MNK / t."""
     import torch
     import block_quantized_integer_gb300 as qg
     from block_quantized_integer_gb300 import inputs
     out = []
-    for i, (M, N, K) in enumerate(inputs.PREFILL_SHAPES):
-        w, x = inputs.prefill_case(M, N, K, sub=i)
+    shapes = inputs.LONGCTX_SHAPES if long_ctx else inputs.PREFILL_SHAPES
+    for i, (M, N, K) in enumerate(shapes):
+        w, x = (inputs.longctx_case(M, N, K, sub=i) if long_ctx
+                else inputs.prefill_case(M, N, K, sub=i))
         qw, dw = qg.quantize_weight_q8_0(torch.from_numpy(w).to(dev))
         qx, dx = qg.quantize_act_q8(torch.from_numpy(x).to(dev))
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -365,7 +368,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
-    ap.add_argument("--only", choices=["prefill", "moe", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "decode"], default=None,
                     help="run one section only (for profiling); prints its JSON")
     ap.add_argument("--reps", type=int, default=20, help="timed calls per prefill/MoE shape")
     args = ap.parse_args()
@@ -376,6 +379,8 @@ def main():
         peaks = load_peaks()
         if args.only == "prefill":
             out = prefill_section(dev, peaks, reps=args.reps)
+        elif args.only == "longctx":
+            out = prefill_section(dev, peaks, reps=args.reps, long_ctx=True)
         elif args.only == "moe":
             out = moe_section(dev, peaks, reps=args.reps)
         else:
@@ -486,6 +491,9 @@ def main():
         del g4, projs4
         torch.cuda.empty_cache()
         line["prefill"] = prefill_section(dev, peaks, reps=args.reps)
+        torch.cuda.empty_cache()
+        line["prefill_long_context"] = prefill_section(dev, peaks, reps=max(args.reps // 4, 3),
+                                                       long_ctx=True)
         torch.cuda.empty_cache()
         line["moe"] = moe_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()

@@ -226,6 +226,36 @@ def test_prefill_full_shape_sampled(shape, algo):
     assert_close(to_np(y)[rows], y_ref, mag)
 
 
+# ------------------------------------------------------------------ full-size long context (sampled)
+
+@pytest.mark.parametrize("shape", inputs.LONGCTX_SHAPES)
+def test_longctx_full_shape_sampled(shape):
+    """M = 18432 through the default path (tensor cores): weights bit-exact on
+    sampled rows, y within tolerance on sampled rows, no device error."""
+    M, N, K = shape
+    i = inputs.LONGCTX_SHAPES.index(shape)
+    w, x = inputs.longctx_case(M, N, K, sub=i)
+    qw, dw = qg.quantize_weight_q8_0(to_dev(w))
+    xt = to_dev(x)
+    qx, dx = qg.quantize_act_q8(xt)
+    del xt
+    y = qg.qgemm_q8_0(qx, dx, qw, dw)
+    _sync()
+    assert qg.device_error() == 0
+    rng = np.random.default_rng(6)
+    rows = np.sort(rng.choice(M, 8, replace=False))
+    rows[-1] = M - 1
+    cols = np.sort(rng.choice(N, 512, replace=False))
+    cols[-1] = N - 1
+    qw_ref, dw_ref = oracle.quantize_w_q8_0(w[cols])
+    assert np.array_equal(to_np(qw[torch.from_numpy(cols).to(dev())]), qw_ref)
+    qx_ref, dx_ref = oracle.quantize_act_q8(x[rows])
+    assert np.array_equal(to_np(qx)[rows], qx_ref)
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref, dw_ref, 8)
+    yg = to_np(y[torch.from_numpy(rows).to(dev())])[:, cols]
+    assert_close(yg, y_ref, mag)
+
+
 # ------------------------------------------------------------------ MoE
 
 def _moe_small(E=9, T=53, topk=3, N=96, K=128, seed=3):
