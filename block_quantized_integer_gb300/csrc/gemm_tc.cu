@@ -13,21 +13,23 @@
 // 2^14 and each group sum an integer below 2^19, which the tensor core
 // accumulates without loss (the group-dot tests check this bit for bit).
 //
-// Per CTA: a 128 x 128 output tile, K walked one 32-group at a time.
+// Per CTA (persistent, one per SM, 704 threads): 128 x 128 output tiles, K
+// walked one pair of 32-groups at a time.
 //   pre-pass    activation codes widened to binary16 once per call (for the
-//               MoE product also gathered into expert order with their scales).
-//   warp 8      TMA producer: binary16 A tiles (2 groups per stage, 128-byte
+//               MoE product also gathered into expert order with their
+//               scales); weight scales transposed to group-major binary32.
+//   warp 16     TMA producer: binary16 A stages (one pair of groups, 128-byte
 //               swizzle, the operand layout the MMA reads directly), int8 or
-//               packed 4-bit B tiles (4 / 8 groups per stage, 128-byte
-//               swizzle), dx / dw scale tiles every 8 groups.
-//   warps 10-11 converters: B codes -> binary16 into the canonical K-major
-//               no-swizzle layout (8 x 16-byte core matrices), one group per
-//               buffer, 4 buffers; dw -> binary32 once per 8 groups.
-//   warp 9      one thread issues two K=16 MMAs per group into one of four
-//               128-column TMEM buffers (the first MMA overwrites).
-//   warps 0-7   epilogue: one tcgen05.ld round trip fetches a group's 64
-//               partials per thread (row = TMEM lane, warpgroup = 64 columns);
-//               the buffer is released at once and y += S * (dx * dw) runs on
+//               packed 4-bit B stages (4 / 8 groups, 128-byte swizzle), dx / dw
+//               scale stages every 8 groups.
+//   warps 18-21 converters, one B row per thread: B codes -> binary16 into
+//               the canonical K-major no-swizzle layout (8 x 16-byte core
+//               matrices), a pair of groups per operand slot, 4 slots.
+//   warp 17     one thread issues, per pair, four K=16 MMAs (two per group,
+//               the first of each overwrites) into one of two 256-column TMEM
+//               pair slots and one commit.
+//   warps 0-15  epilogue: 16-lane x 256-bit TMEM reads, the pair slot is
+//               released as soon as it is read, then y += (S * dw) * dx on
 //               packed f32x2 instructions into binary32 registers.
 // Every mbarrier wait is bounded; on a timeout the CTA sets a device error
 // word, drains its own TMA copies and MMAs, frees TMEM and returns.
@@ -53,16 +55,16 @@ constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumu
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
-constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 2;
+constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 4;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 640
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704: 88 registers a thread
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
 constexpr int F16_B = BN * 32 * 2;                   // 8192: one group of binary16 B
 constexpr int F16_PAIR = 2 * F16_B;                  // 16384
-constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [8][128] f32 (dense) or [128][8] (grouped)
-constexpr int SC_DW = SCG * BN * 4;                  // 4096: dw [8][128] f32 (transposed)
+constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128 rows][8 groups] f32
+constexpr int SC_DW = SCG * BN * 4;                  // 4096: dw [8 groups][128 columns] f32, permuted
 constexpr int SC_STAGE = SC_DX + SC_DW;              // 8192
 
 constexpr int OFF_A = 0;
@@ -70,7 +72,7 @@ constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
 constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NP + 2 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + NP + 2 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -82,21 +84,22 @@ constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
 constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
 constexpr uint32_t kSleepHintNs = 20000;             // a waiter sleeps until the phase flips
 
-// full_a: TMA A stage landed; full_f16: converters wrote the B pair; ops_free:
-// the MMAs that read an operand slot completed (one commit frees A and B).
+// full_a: TMA A stage landed; full_ops: the converters saw full_a and wrote
+// the binary16 B pair, so both operands of the slot are ready; done: the
+// MMAs of the pair completed (one commit: operand slot free and the pair's
+// accumulators readable); tempty: the epilogue has read the TMEM pair slot.
 struct Bars {
-    uint32_t full_a, full_f16, ops_free, full_b, empty_b, tfull, tempty, full_sc, empty_sc, drain;
+    uint32_t full_a, full_ops, done, full_b, empty_b, tempty, full_sc, empty_sc, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
     Bars b;
     b.full_a = base;
-    b.full_f16 = b.full_a + 8 * NO;
-    b.ops_free = b.full_f16 + 8 * NO;
-    b.full_b = b.ops_free + 8 * NO;
+    b.full_ops = b.full_a + 8 * NO;
+    b.done = b.full_ops + 8 * NO;
+    b.full_b = b.done + 8 * NO;
     b.empty_b = b.full_b + 8 * NB;
-    b.tfull = b.empty_b + 8 * NB;
-    b.tempty = b.tfull + 8 * NP;
+    b.tempty = b.empty_b + 8 * NB;
     b.full_sc = b.tempty + 8 * NP;
     b.empty_sc = b.full_sc + 8 * NSC;
     b.drain = b.empty_sc + 8 * NSC;
@@ -160,46 +163,53 @@ __device__ __forceinline__ uint32_t u4x2_to_h2(uint32_t nib_bytes, uint32_t sel)
     return r;
 }
 
-// Group gi (0 .. GB-1) of the int8 / packed 4-bit B stage -> binary16 B buffer
+// Groups gi, gi + 1 of the int8 / packed 4-bit B stage -> the binary16 B pair
 // (canonical no-swizzle K-major layout: core matrix (row/8, k8) at
-// (row/8)*512 + k8*128, row%8 at +16 each).
+// (row/8)*512 + k8*128, row%8 at +16 each; the second group F16_B further).
+// Thread ct owns B row ct; all its shared loads go out before any store.
 template <bool kQ4>
-__device__ __forceinline__ void convert_group(const uint8_t* src, uint8_t* dst, int gi, int ct) {
+__device__ __forceinline__ void convert_pair(const uint8_t* src, uint8_t* dst, int gi, int ct) {
+    static_assert(CONV_THREADS == BN, "one converter thread per B row");
+    const int row = ct, sw = row & 7;
+    const uint8_t* srow = src + row * 128;
+    uint8_t* drow = dst + (row >> 3) * 512 + sw * 16;
     if constexpr (!kQ4) {
-#pragma unroll 2
-        for (int j = 0; j < BN * 2 / CONV_THREADS; ++j) {
-            const int i = ct + j * CONV_THREADS;
-            const int row = i & (BN - 1), half = i >> 7;
-            const int chunk = gi * 2 + half;          // 128-byte swizzle: chunk ^ (row & 7)
-            const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((chunk ^ (row & 7)) << 4));
+        uint4 v[4];                                    // chunks 2 gi .. 2 gi + 3 (16 codes each)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            v[c] = *reinterpret_cast<const uint4*>(srow + (((2 * gi + c) ^ sw) << 4));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
             uint4 lo, hi;
-            s8x16_to_h16(v, lo, hi);
-            uint8_t* o = dst + (row >> 3) * 512 + (half * 2) * 128 + (row & 7) * 16;
+            s8x16_to_h16(v[c], lo, hi);
+            uint8_t* o = drow + (c >> 1) * F16_B + (c & 1) * 256;
             *reinterpret_cast<uint4*>(o) = lo;
             *reinterpret_cast<uint4*>(o + 128) = hi;
         }
     } else {
+        uint4 v[2];                                    // one 16-byte group each
 #pragma unroll
-      for (int j = 0; j < BN / CONV_THREADS; ++j) {
-        const int row = ct + j * CONV_THREADS;        // one 16-byte group per row
-        const uint4 v = *reinterpret_cast<const uint4*>(src + row * 128 + ((gi ^ (row & 7)) << 4));
-        // byte j: element j (low nibble), element j+16 (high nibble)
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t lo_h[8], hi_h[8];
+        for (int c = 0; c < 2; ++c)
+            v[c] = *reinterpret_cast<const uint4*>(srow + (((gi + c) ^ sw) << 4));
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
-            lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
-            lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
-            hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
-            hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+        for (int c = 0; c < 2; ++c) {
+            // byte j: element j (low nibble), element j+16 (high nibble)
+            const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+            uint32_t lo_h[8], hi_h[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+                lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+                lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+                hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+                hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+            }
+            uint8_t* o = drow + c * F16_B;
+            *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+            *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+            *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+            *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
         }
-        uint8_t* o = dst + (row >> 3) * 512 + (row & 7) * 16;
-        *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
-        *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
-        *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
-        *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
-      }
     }
 }
 
@@ -247,7 +257,7 @@ template <bool kQ4, bool kGrouped>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
-               float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec4,
+               float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec2,
                GroupedArgs ga, int n_tiles, int64_t dense_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -265,17 +275,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (tid == 0) {
         for (int i = 0; i < NO; ++i) {
             mbar_init(B.full_a + 8 * i, 1);
-            mbar_init(B.full_f16 + 8 * i, CONV_WARPS);
-            mbar_init(B.ops_free + 8 * i, 1);
+            mbar_init(B.full_ops + 8 * i, CONV_WARPS);
+            mbar_init(B.done + 8 * i, 1);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NP; ++i) {
-            mbar_init(B.tfull + 8 * i, 1);
-            mbar_init(B.tempty + 8 * i, EPI_WARPS);
-        }
+        for (int i = 0; i < NP; ++i) mbar_init(B.tempty + 8 * i, EPI_WARPS);
         for (int i = 0; i < NSC; ++i) {
             mbar_init(B.full_sc + 8 * i, 1);
             mbar_init(B.empty_sc + 8 * i, EPI_WARPS);
@@ -313,12 +320,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
                         const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
                         mbar_expect_tx(B.full_sc + 8 * slot, SC_STAGE);
-                        // dense: dx transposed (x = first row, a multiple of 128);
-                        // grouped: dx row-major (segment starts are arbitrary rows)
-                        if constexpr (kGrouped)
-                            tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
-                        else
-                            tma_load_2d(dst, &map_dx, (int32_t)T.m0, g, B.full_sc + 8 * slot);
+                        // dx row-major [rows][G]: x = g, a multiple of 8 groups (32 bytes)
+                        tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
                         tma_load_2d(dst + SC_DX, &map_dw, (int32_t)T.n0, (int32_t)(T.sg0 + g),
                                     B.full_sc + 8 * slot);
                         ++isc;
@@ -333,7 +336,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     }
                     if (g % GA == 0) {
                         const int slot = (int)(ia % NO);
-                        if (!(ok = wait_bar<false>(B.ops_free + 8 * slot, ((ia / NO) & 1) ^ 1, abort))) break;
+                        if (!(ok = wait_bar<false>(B.done + 8 * slot, ((ia / NO) & 1) ^ 1, abort))) break;
                         mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
                         tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, g * 32, (int32_t)T.m0,
                                     B.full_a + 8 * slot);
@@ -359,13 +362,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 for (int pl = 0; pl < PAIRS; ++pl, ++p) {
                     const int so = (int)(p % NO), ps = (int)(p % NP);
                     const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
-                    // the three probes go out back to back; one branch on all of them
-                    const bool ready = mbar_try_wait(B.full_a + 8 * so, po) &
-                                       mbar_try_wait(B.full_f16 + 8 * so, po) &
+                    // both probes go out back to back; one branch on the pair
+                    const bool ready = mbar_try_wait(B.full_ops + 8 * so, po) &
                                        mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
                     if (!ready) {
-                        if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
-                        if (!(ok = wait_bar<false>(B.full_f16 + 8 * so, po, abort))) break;
+                        if (!(ok = wait_bar<false>(B.full_ops + 8 * so, po, abort))) break;
                         if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
                     }
                     tc_fence_after();
@@ -378,8 +379,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         for (int j = 0; j < 2; ++j)
                             mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
                                     smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
-                    mma_commit(B.tfull + 8 * ps);
-                    mma_commit(B.ops_free + 8 * so);
+                    mma_commit(B.done + 8 * so);
                     issued_any = true;
                 }
             }
@@ -399,15 +399,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 if (g0 % GB == 0 && !(ok = wait_bar<true>(B.full_b + 8 * (sb % NB), (sb / NB) & 1, abort))) break;
                 // the operand slot is free once the MMAs of pair p - NO completed
                 const int so = (int)(p % NO);
-                if (!(ok = wait_bar<true>(B.ops_free + 8 * so, (uint32_t)(((p / NO) & 1) ^ 1), abort))) break;
+                if (!(ok = wait_bar<true>(B.done + 8 * so, (uint32_t)(((p / NO) & 1) ^ 1), abort))) break;
                 const uint8_t* src = smem + OFF_B + (sb % NB) * B_STAGE;
                 uint8_t* dst = smem + OFF_F16 + so * F16_PAIR;
-                convert_group<kQ4>(src, dst, g0 % GB, ct);
-                convert_group<kQ4>(src, dst + F16_B, (g0 + 1) % GB, ct);
+                convert_pair<kQ4>(src, dst, g0 % GB, ct);
                 fence_proxy_async_smem();
+                // the A stage of the slot has landed too: full_ops then stands for both
+                if (!(ok = wait_bar<true>(B.full_a + 8 * so, (uint32_t)((p / NO) & 1), abort))) break;
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(B.full_f16 + 8 * so);
+                    mbar_arrive(B.full_ops + 8 * so);
                     if ((g0 + 1) % GB == GB - 1) mbar_arrive(B.empty_b + 8 * (sb % NB));
                 }
                 if ((g0 + 1) % GB == GB - 1) ++sb;
@@ -415,54 +416,77 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // TMEM is read in 16-lane x 256-bit fragments: per 8-column block a
+        // thread holds 2 adjacent columns of 2 rows (8 rows apart), so one
+        // binary32 pair of dw and one dx serve 2 partials each, and the column
+        // pairs go through packed f32x2 multiplies and FMAs.  Warp w covers
+        // the 32 rows of its TMEM lane quarter (w % 4) and 32 columns.  The
+        // dw stage holds each 32-column block permuted so that a thread's 8
+        // columns (4 blocks x 2) are contiguous: 2 x 16-byte loads per group.
         const int q = warp & 3;                             // TMEM lane quarter
-        const int row = q * 32 + lane;
         const int cb = (warp >> 2) * 32;                    // 32 columns per warp
+        const int c2 = 2 * (lane & 3);
+        const int rb = q * 32 + (lane >> 2);                // rows rb + 8 i, i = 0..3
         uint32_t p = 0, sc = 0;
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
-            float acc[32];
+            // a quarter with no valid row (short MoE segments, ragged last
+            // tile) keeps the barrier protocol but skips the readout and math
+            const bool live = q * 32 < tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+            uint64_t acc[4][4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
             for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                const int g0 = 2 * pl, ps = (int)(p % NP);
+                const int g0 = 2 * pl, ps = (int)(p % NP), so = (int)(p % NO);
                 const int slot = (int)(sc % NSC);
                 if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
-                if (!(ok = wait_bar<true>(B.tfull + 8 * ps, (uint32_t)((p / NP) & 1), abort))) break;
+                if (!(ok = wait_bar<true>(B.done + 8 * so, (uint32_t)((p / NO) & 1), abort))) break;
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * BN + cb);
-                const uint8_t* st = smem + OFF_SC + slot * SC_STAGE;
-                float2 dxv;
-                if constexpr (kGrouped) {
-                    dxv = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(st) +
-                                                           row * SCG + (g0 % SCG));
-                } else {                                    // contiguous over the warp's rows
-                    const float* dxt = reinterpret_cast<const float*>(st) + (g0 % SCG) * BM + row;
-                    dxv = make_float2(dxt[0], dxt[BM]);
-                }
-                const float* dw0 = reinterpret_cast<const float*>(st + SC_DX) + (g0 % SCG) * BN + cb;
-                // the two groups of the pair one after the other (32 partials live);
-                // the other warps on this SMSP cover the TMEM latency
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sv[32];
-                    tmem_ld32(taddr + h * BN, sv);
-                    tmem_wait_ld();
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
-                    }
-                    const float dh = h ? dxv.y : dxv.x;
-                    const float* dwh = dw0 + h * BN;
+                if (live) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)(ps * 2 * BN + cb);
+                    const float* scf = reinterpret_cast<const float*>(smem + OFF_SC + slot * SC_STAGE);
+                    // dx of the pair's two groups, adjacent in the row-major stage
+                    float2 dxp[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 w = *reinterpret_cast<const float4*>(dwh + i * 4);
-                        acc[4 * i + 0] = fmaf(__uint_as_float(sv[4 * i + 0]), dh * w.x, acc[4 * i + 0]);
-                        acc[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), dh * w.y, acc[4 * i + 1]);
-                        acc[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), dh * w.z, acc[4 * i + 2]);
-                        acc[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), dh * w.w, acc[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i)
+                        dxp[i] = *reinterpret_cast<const float2*>(scf + (rb + 8 * i) * SCG + (g0 % SCG));
+                    const float* dwp = scf + SC_DX / 4 + (g0 % SCG) * BN + cb + 4 * c2;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // this thread's 8 dw of group g0 + h: pairs for column blocks 0..3
+                        const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(dwp + h * BN);
+                        const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(dwp + h * BN + 4);
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {                  // 16-column halves
+                            const uint32_t ta = taddr + h * BN + 16 * k;
+                            uint32_t s0[8], s1[8];
+                            tmem_ld16x256b_x2(ta, s0);                 // rows rb, rb + 8
+                            tmem_ld16x256b_x2(ta + (16u << 16), s1);   // rows rb + 16, rb + 24
+                            tmem_wait_ld();
+                            if (h == 1 && k == 1) {                    // pair slot read out
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                            }
+                            const uint64_t w0 = k ? wb.x : wa.x, w1 = k ? wb.y : wa.y;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float d = h ? dxp[i].y : dxp[i].x;
+                                const uint64_t dx2 = pack2(d, d);
+                                const uint32_t* sv = i < 2 ? s0 : s1;
+                                const int e = 2 * (i & 1);
+                                fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), w0), dx2);
+                                fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), w1), dx2);
+                            }
+                        }
                     }
+                } else {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
                 }
                 if ((g0 + 1) % SCG == SCG - 1) {
                     __syncwarp();
@@ -471,22 +495,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 }
             }
             if (!ok) break;
-            const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
-            if (row < T.rows) {
-                int64_t orow;
-                if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
-                else orow = T.m0 + row;
-                float* yr = y + orow * ldy + T.n0 + cb;
-                const int64_t ncols = N - (T.n0 + cb);
-                if (vec4 && ncols >= 32) {
+            if (live) {
+                const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
+                const int64_t col0 = T.n0 + cb + c2;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<float4*>(yr + 4 * i) =
-                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-                } else {
+                for (int i = 0; i < 4; ++i) {
+                    const int row = rb + 8 * i;                       // tile row
+                    if (row < T.rows) {
+                        int64_t orow;
+                        if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
+                        else orow = T.m0 + row;
+                        float* yr = y + orow * ldy + col0;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < ncols) yr[i] = acc[i];
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 v = unpack2(acc[i][j]);
+                            const int64_t col = col0 + 8 * j;
+                            if (vec2 && col + 1 < N) {
+                                *reinterpret_cast<float2*>(yr + 8 * j) = v;
+                            } else {
+                                if (col < N) yr[8 * j] = v.x;
+                                if (col + 1 < N) yr[8 * j + 1] = v.y;
+                            }
+                        }
+                    }
                 }
             }
         }
@@ -531,31 +562,23 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
     }
 }
 
-// dwT[r][n] = float(dw[n][g]) with r = e * G + g: the scale plane transposed to
-// group-major binary32 rows of ldt columns, the layout the epilogue reads.
+// dwT[r][.] with r = e * G + g: the scale plane transposed to group-major
+// binary32 rows of ldt columns (ldt a multiple of 32), the layout the
+// epilogue reads.  Inside each 32-column block, column 8j + 2c + e is stored
+// at 8c + 2j + e (j, c < 4, e < 2), so the 8 columns one epilogue thread
+// scales are contiguous; columns past N are stored as zero.
 __global__ void __launch_bounds__(256)
 transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t G, int64_t E,
                         float* __restrict__ dwt, int64_t ldt) {
-    const int64_t total = E * rows_n * G;
+    const int64_t total = E * ldt * G;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        // i walks dwT in order: e, g, n (coalesced writes)
-        const int64_t n = i % rows_n, eg = i / rows_n;
+        // i walks dwT in storage order: e, g, stored column (coalesced writes)
+        const int64_t sidx = i % ldt, eg = i / ldt;
         const int64_t g = eg % G, e = eg / G;
-        dwt[eg * ldt + n] = half_bits_to_float(dw[(e * rows_n + n) * G + g]);
-    }
-}
-
-// dxt[g][m] = dx[m][g]: activation scales transposed to group-major rows of
-// ldm columns, so the epilogue's 32 rows of one group are contiguous.
-__global__ void __launch_bounds__(256)
-transpose_dx_kernel(const float* __restrict__ dx, int64_t M, int64_t G, float* __restrict__ dxt,
-                    int64_t ldm) {
-    const int64_t total = M * G;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t m = i % M, g = i / M;               // writes coalesced along m
-        dxt[g * ldm + m] = dx[m * G + g];
+        const int r = (int)(sidx & 31), c = r >> 3, j = (r >> 1) & 3, el = r & 1;
+        const int64_t n = (sidx & ~(int64_t)31) + 8 * j + 2 * c + el;
+        dwt[eg * ldt + sidx] = n < rows_n ? half_bits_to_float(dw[(e * rows_n + n) * G + g]) : 0.f;
     }
 }
 
@@ -596,25 +619,19 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 // Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
-// dx [rows][G], transposed scales dwT [E*G][ldt] (binary32, n columns used).
-// ldm > 0: dx is the transposed plane dxt [G][ldm]; ldm == 0: dx is [rows][G].
+// dx [rows][G] (binary32, row-major), scales dwT [E*G][ldt] (binary32).
 bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
                const void* a16, const void* qw, const float* dx, const float* dwt,
-               int64_t rows, int64_t brows, int64_t n, int64_t ldt, int64_t sgrows, int64_t K,
-               bool q4, int64_t ldm) {
+               int64_t rows, int64_t brows, int64_t ldt, int64_t sgrows, int64_t K, bool q4) {
     const int64_t G = K / kGroup;
     const int64_t wbytes = q4 ? K / 2 : K;
-    const bool dx_ok = ldm > 0
-        ? make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, rows, G, ldm * 4, BM, SCG,
-                   CU_TENSOR_MAP_SWIZZLE_NONE)
-        : make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!dx_ok) return false;
-    return make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
+    return make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dwt, n, sgrows, ldt * 4, BN, SCG,
+           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dwt, ldt, sgrows, ldt * 4, BN, SCG,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -626,9 +643,9 @@ cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& m
     cudaError_t e = ensure_smem_attr((const void*)tc_gemm_kernel<kQ4, kGrouped>, SMEM_BYTES,
                                      9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
     if (e != cudaSuccess) return e;
-    const bool vec4 = ((uintptr_t)y % 16 == 0) && (ldy % 4 == 0);
+    const bool vec2 = ((uintptr_t)y % 8 == 0) && (ldy % 2 == 0);
     tc_gemm_kernel<kQ4, kGrouped><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
-                                                                    ldy, vec4, ga, n_tiles,
+                                                                    ldy, vec2, ga, n_tiles,
                                                                     dense_tiles);
     return cudaGetLastError();
 }
@@ -652,31 +669,28 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const vo
            encoder() != nullptr;
 }
 
-int64_t ldt_of(int64_t N) { return (N + 3) / 4 * 4; }
+int64_t ldt_of(int64_t N) { return (N + 31) / 32 * 32; }
 
-// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32 | dxT [G][ldt(M)] binary32
+// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
     const int64_t G = K / kGroup;
-    return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4) +
-           align16((size_t)G * ldt_of(M) * 4);
+    return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4);
 }
 
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s) {
-    const int64_t G = K / kGroup, ldt = ldt_of(N), ldm = ldt_of(M);
+    const int64_t G = K / kGroup, ldt = ldt_of(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* a16 = reinterpret_cast<__half*>(ws);
     float* dwt = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2));
-    float* dxt = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2) + align16((size_t)G * ldt * 4));
     widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
                                                                nullptr, 1, 0);
-    transpose_scales_kernel<<<widen_grid(N * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
-    transpose_dx_kernel<<<widen_grid(M * G), 256, 0, s>>>(dx, M, G, dxt, ldm);
+    transpose_scales_kernel<<<widen_grid(ldt * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dxt, dwt, M, N, N, ldt, G, K, q4, ldm))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, ldt, G, K, q4))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
@@ -709,12 +723,12 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     // gather + widen the routed rows (count read on the device: offsets[E])
     widen_rows_kernel<<<widen_grid(P * (K / 16)), 256, 0, s>>>(qx, dx, P, K, a16, dxg, perm,
                                                                offsets + E, topk, x_row_mode);
-    transpose_scales_kernel<<<widen_grid((int64_t)E * N * G), 256, 0, s>>>(dw, N, G, E, dwt, ldt);
+    transpose_scales_kernel<<<widen_grid((int64_t)E * ldt * G), 256, 0, s>>>(dw, N, G, E, dwt, ldt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dwt, P, (int64_t)E * N, N, ldt,
-                   (int64_t)E * G, K, true, 0))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dwt, P, (int64_t)E * N, ldt,
+                   (int64_t)E * G, K, true))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     GroupedArgs ga{perm, offsets, tile_offsets, E, N};

@@ -73,9 +73,8 @@ const char* qg_status_string(qg_status s);
 /* Bytes of device workspace the given call needs (0 if none).  For the dense
  * GEMMs pass M, N, K (T, topk, E ignored): M > 8 with K % 256 == 0 runs on the
  * tensor cores and needs M*K*2 bytes (activation codes widened to binary16)
- * plus (K/32)*ceil4(N)*4 bytes (weight scales transposed to binary32) plus
- * (K/32)*ceil4(M)*4 bytes (activation scales transposed), each part padded to
- * 16 bytes; QG_ALGO_TCGEN05 chosen explicitly needs the same
+ * plus (K/32)*ceil32(N)*4 bytes (weight scales transposed to binary32), each
+ * part padded to 16 bytes; QG_ALGO_TCGEN05 chosen explicitly needs the same
  * for any M (take the size for M = 9 as the floor).  For the MoE GEMM pass K and N and the routing sizes T, topk, E
  * (M ignored).  Workspace pointers must be 16-byte aligned. */
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,
