@@ -57,15 +57,18 @@ constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
 constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 4;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704: 88 registers a thread
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704: 80 registers a thread
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
 constexpr int F16_B = BN * 32 * 2;                   // 8192: one group of binary16 B
 constexpr int F16_PAIR = 2 * F16_B;                  // 16384
-constexpr int SC_DX = BM * SCG * 4;                  // 4096: dx [128 rows][8 groups] f32
-constexpr int SC_DW = SCG * BN * 4;                  // 4096: dw [8 groups][128 columns] f32, permuted
+// scale stage: dx [128 rows][8 groups] f32, then dw: dense [8 groups][128
+// columns] f32 (permuted), MoE [128 rows][8 groups] binary16.
+constexpr int SC_DX = BM * SCG * 4;                  // 4096
+constexpr int SC_DW = SCG * BN * 4;                  // 4096
 constexpr int SC_STAGE = SC_DX + SC_DW;              // 8192
+constexpr int SC_DW16 = BN * SCG * 2;                // 2048: MoE dw
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NO * A_STAGE;
@@ -217,6 +220,7 @@ struct GroupedArgs {
     const int32_t* perm;          // sorted position -> pair index
     const int32_t* offsets;       // [E+1]
     const int32_t* tile_offsets;  // [E+1] in 128-row tiles
+    const int4* tile_info;        // per 128-row tile: {first sorted row, rows, expert, 0}
     int32_t E;
     int64_t N;                    // per-expert output columns
 };
@@ -233,15 +237,11 @@ __device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, int G, const Group
     const int64_t mt = t / n_tiles;
     T.n0 = (t % n_tiles) * BN;
     if constexpr (kGrouped) {
-        int lo = 0, hi = ga.E - 1;                       // last e with tile_offsets[e] <= mt
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (ga.tile_offsets[mid] <= mt) lo = mid; else hi = mid - 1;
-        }
-        T.m0 = ga.offsets[lo] + (mt - ga.tile_offsets[lo]) * BM;
-        T.rows = min64(BM, (int64_t)ga.offsets[lo + 1] - T.m0);
-        T.bn0 = (int64_t)lo * ga.N + T.n0;
-        T.sg0 = (int64_t)lo * G;
+        const int4 info = ga.tile_info[mt];
+        T.m0 = info.x;
+        T.rows = info.y;
+        T.bn0 = (int64_t)info.z * ga.N + T.n0;
+        T.sg0 = (int64_t)info.z * G;
     } else {
         T.m0 = mt * BM;
         T.rows = min64(BM, M - T.m0);
@@ -319,11 +319,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         const int slot = (int)(isc % NSC);
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
                         const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
-                        mbar_expect_tx(B.full_sc + 8 * slot, SC_STAGE);
+                        mbar_expect_tx(B.full_sc + 8 * slot, kGrouped ? SC_DX + SC_DW16 : SC_STAGE);
                         // dx row-major [rows][G]: x = g, a multiple of 8 groups (32 bytes)
                         tma_load_2d(dst, &map_dx, g, (int32_t)T.m0, B.full_sc + 8 * slot);
-                        tma_load_2d(dst + SC_DX, &map_dw, (int32_t)T.n0, (int32_t)(T.sg0 + g),
-                                    B.full_sc + 8 * slot);
+                        if constexpr (kGrouped)        // dw binary16 [E*N][G] as stored: x = g (16 bytes)
+                            tma_load_2d(dst + SC_DX, &map_dw, g, (int32_t)T.bn0, B.full_sc + 8 * slot);
+                        else                           // dwT binary32 [G][ldt], permuted columns
+                            tma_load_2d(dst + SC_DX, &map_dw, (int32_t)T.n0, (int32_t)(T.sg0 + g),
+                                        B.full_sc + 8 * slot);
                         ++isc;
                     }
                     if (g % GB == 0) {
@@ -358,7 +361,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (lane == 0) {
             bool issued_any = false, ok = true;
             uint32_t p = 0;                                 // pair counter (A stage = pair)
+            // MoE tiles put the 128 weight rows on the MMA's M side (TMEM lanes)
+            // and the segment's rows on N, rounded up to 16: short segments
+            // cost short MMAs.  The next tile's row count is fetched a tile early.
+            int next_rows = (kGrouped && t0 < num_tiles) ? tile_at<kGrouped>(t0, M, G, ga, n_tiles).rows : BM;
             for (int t = t0; t < num_tiles && ok; t += dt) {
+                uint32_t idesc = IDESC;
+                if constexpr (kGrouped) {
+                    const int nt = min(BM, max(16, (next_rows + 15) & ~15));
+                    idesc = idesc_f16_f32(BN, nt);
+                    if (t + dt < num_tiles) next_rows = tile_at<kGrouped>(t + dt, M, G, ga, n_tiles).rows;
+                }
                 for (int pl = 0; pl < PAIRS; ++pl, ++p) {
                     const int so = (int)(p % NO), ps = (int)(p % NP);
                     const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
@@ -376,9 +389,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int j = 0; j < 2; ++j)
-                            mma_f16(d + h * BN, smem_desc_sw128(a_s + h * 64 + j * 32),
-                                    smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512), IDESC, j);
+                        for (int j = 0; j < 2; ++j) {
+                            const uint64_t da = smem_desc_sw128(a_s + h * 64 + j * 32);
+                            const uint64_t db = smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512);
+                            if constexpr (kGrouped) mma_f16(d + h * BN, db, da, idesc, j);
+                            else mma_f16(d + h * BN, da, db, idesc, j);
+                        }
                     mma_commit(B.done + 8 * so);
                     issued_any = true;
                 }
@@ -417,22 +433,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     } else {
         // ------------------------------------------------------------ epilogue
         // TMEM is read in 16-lane x 256-bit fragments: per 8-column block a
-        // thread holds 2 adjacent columns of 2 rows (8 rows apart), so one
-        // binary32 pair of dw and one dx serve 2 partials each, and the column
-        // pairs go through packed f32x2 multiplies and FMAs.  Warp w covers
-        // the 32 rows of its TMEM lane quarter (w % 4) and 32 columns.  The
-        // dw stage holds each 32-column block permuted so that a thread's 8
-        // columns (4 blocks x 2) are contiguous: 2 x 16-byte loads per group.
+        // thread holds 2 adjacent columns of 2 lanes (8 apart), so each scale
+        // pair serves 2 partials, and the column pairs go through packed
+        // f32x2 multiplies and FMAs.  Warp w covers the 32 lanes of its TMEM
+        // quarter (w % 4) and 32 columns.
+        //   dense: lanes = A rows (dx per lane), columns = B rows (dw per
+        //     column; the dw stage holds each 32-column block permuted so that
+        //     a thread's 8 columns are contiguous: 2 x 16-byte loads a group);
+        //   MoE: lanes = weight rows (dw per lane, binary16 as stored),
+        //     columns = the segment's rows (dx per column).
+        // Both compute y += (S * dw) * dx with the same roundings.
         const int q = warp & 3;                             // TMEM lane quarter
         const int cb = (warp >> 2) * 32;                    // 32 columns per warp
         const int c2 = 2 * (lane & 3);
-        const int rb = q * 32 + (lane >> 2);                // rows rb + 8 i, i = 0..3
+        const int rb = q * 32 + (lane >> 2);                // lanes rb + 8 i, i = 0..3
         uint32_t p = 0, sc = 0;
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
-            // a quarter with no valid row (short MoE segments, ragged last
+            // a warp with no valid output (short MoE segments, ragged last
             // tile) keeps the barrier protocol but skips the readout and math
-            const bool live = q * 32 < tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+            const int trows = (int)tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+            const bool live = kGrouped ? cb < trows : q * 32 < trows;
             uint64_t acc[4][4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -448,38 +469,56 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
                                            (uint32_t)(ps * 2 * BN + cb);
                     const float* scf = reinterpret_cast<const float*>(smem + OFF_SC + slot * SC_STAGE);
-                    // dx of the pair's two groups, adjacent in the row-major stage
-                    float2 dxp[4];
+                    // per-lane scales of the pair's two groups
+                    float2 lsc[4];
+                    if constexpr (kGrouped) {
+                        const __half2* dws = reinterpret_cast<const __half2*>(smem + OFF_SC + slot * SC_STAGE + SC_DX);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dxp[i] = *reinterpret_cast<const float2*>(scf + (rb + 8 * i) * SCG + (g0 % SCG));
-                    const float* dwp = scf + SC_DX / 4 + (g0 % SCG) * BN + cb + 4 * c2;
+                        for (int i = 0; i < 4; ++i) lsc[i] = __half22float2(dws[((rb + 8 * i) * SCG + (g0 % SCG)) / 2]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            lsc[i] = *reinterpret_cast<const float2*>(scf + (rb + 8 * i) * SCG + (g0 % SCG));
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        // this thread's 8 dw of group g0 + h: pairs for column blocks 0..3
-                        const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(dwp + h * BN);
-                        const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(dwp + h * BN + 4);
+                        // per-column scale pairs of group g0 + h for column blocks 0..3
+                        uint64_t csc[4];
+                        if constexpr (kGrouped) {
+                            const float* dxc = scf + (cb + c2) * SCG + (g0 % SCG) + h;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) csc[j] = pack2(dxc[8 * j * SCG], dxc[(8 * j + 1) * SCG]);
+                        } else {
+                            const float* dwp = scf + SC_DX / 4 + ((g0 % SCG) + h) * BN + cb + 4 * c2;
+                            const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(dwp);
+                            const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(dwp + 4);
+                            csc[0] = wa.x; csc[1] = wa.y; csc[2] = wb.x; csc[3] = wb.y;
+                        }
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {                  // 16-column halves
                             const uint32_t ta = taddr + h * BN + 16 * k;
                             uint32_t s0[8], s1[8];
-                            tmem_ld16x256b_x2(ta, s0);                 // rows rb, rb + 8
-                            tmem_ld16x256b_x2(ta + (16u << 16), s1);   // rows rb + 16, rb + 24
+                            tmem_ld16x256b_x2(ta, s0);                 // lanes rb, rb + 8
+                            tmem_ld16x256b_x2(ta + (16u << 16), s1);   // lanes rb + 16, rb + 24
                             tmem_wait_ld();
                             if (h == 1 && k == 1) {                    // pair slot read out
                                 tc_fence_before();
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
                             }
-                            const uint64_t w0 = k ? wb.x : wa.x, w1 = k ? wb.y : wa.y;
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const float d = h ? dxp[i].y : dxp[i].x;
-                                const uint64_t dx2 = pack2(d, d);
+                                const float d = h ? lsc[i].y : lsc[i].x;
+                                const uint64_t d2 = pack2(d, d);
                                 const uint32_t* sv = i < 2 ? s0 : s1;
                                 const int e = 2 * (i & 1);
-                                fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), w0), dx2);
-                                fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), w1), dx2);
+                                if constexpr (kGrouped) {
+                                    fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), d2), csc[2 * k]);
+                                    fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), d2), csc[2 * k + 1]);
+                                } else {
+                                    fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), csc[2 * k]), d2);
+                                    fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), csc[2 * k + 1]), d2);
+                                }
                             }
                         }
                     }
@@ -497,24 +536,39 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             if (!ok) break;
             if (live) {
                 const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
-                const int64_t col0 = T.n0 + cb + c2;
+                if constexpr (kGrouped) {
+                    // lane rb + 8 i = output column n0 + rb + 8 i; column = segment row
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = rb + 8 * i;                       // tile row
-                    if (row < T.rows) {
-                        int64_t orow;
-                        if constexpr (kGrouped) orow = ga.perm[T.m0 + row];
-                        else orow = T.m0 + row;
-                        float* yr = y + orow * ldy + col0;
+                    for (int j = 0; j < 4; ++j)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float2 v = unpack2(acc[i][j]);
-                            const int64_t col = col0 + 8 * j;
-                            if (vec2 && col + 1 < N) {
-                                *reinterpret_cast<float2*>(yr + 8 * j) = v;
-                            } else {
-                                if (col < N) yr[8 * j] = v.x;
-                                if (col + 1 < N) yr[8 * j + 1] = v.y;
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = cb + 8 * j + c2 + e;
+                            if (r < T.rows) {
+                                float* yr = y + (int64_t)ga.perm[T.m0 + r] * ldy + T.n0;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 v = unpack2(acc[i][j]);
+                                    if (T.n0 + rb + 8 * i < N) yr[rb + 8 * i] = e ? v.y : v.x;
+                                }
+                            }
+                        }
+                } else {
+                    const int64_t col0 = T.n0 + cb + c2;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = rb + 8 * i;                   // tile row
+                        if (row < T.rows) {
+                            float* yr = y + (T.m0 + row) * ldy + col0;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 v = unpack2(acc[i][j]);
+                                const int64_t col = col0 + 8 * j;
+                                if (vec2 && col + 1 < N) {
+                                    *reinterpret_cast<float2*>(yr + 8 * j) = v;
+                                } else {
+                                    if (col < N) yr[8 * j] = v.x;
+                                    if (col + 1 < N) yr[8 * j + 1] = v.y;
+                                }
                             }
                         }
                     }
@@ -582,6 +636,19 @@ transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t
     }
 }
 
+// MoE tile table: m-tile t of expert e (tile_offsets[e] <= t < tile_offsets[e+1])
+// covers sorted rows offsets[e] + (t - tile_offsets[e]) * BM onward.
+__global__ void __launch_bounds__(128)
+tile_info_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_offsets,
+                 int32_t E, int4* __restrict__ info) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+        const int32_t end = offsets[e + 1];
+        int32_t m0 = offsets[e];
+        for (int32_t t = tile_offsets[e]; t < tile_offsets[e + 1]; ++t, m0 += BM)
+            info[t] = make_int4(m0, min(BM, end - m0), e, 0);
+    }
+}
+
 // ---- host side ----------------------------------------------------------------------
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -619,20 +686,25 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 // Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
-// dx [rows][G] (binary32, row-major), scales dwT [E*G][ldt] (binary32).
+// dx [rows][G] (binary32, row-major) and the weight scales: dense, dwT
+// [G][ldt] binary32 (ldt > 0); MoE (ldt == 0), dw [brows][G] binary16 as stored.
 bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
-               const void* a16, const void* qw, const float* dx, const float* dwt,
-               int64_t rows, int64_t brows, int64_t ldt, int64_t sgrows, int64_t K, bool q4) {
+               const void* a16, const void* qw, const float* dx, const void* dws,
+               int64_t rows, int64_t brows, int64_t ldt, int64_t K, bool q4) {
     const int64_t G = K / kGroup;
     const int64_t wbytes = q4 ? K / 2 : K;
-    return make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
+    const bool dw_ok = ldt > 0
+        ? make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dws, ldt, G, ldt * 4, BN, SCG,
+                   CU_TENSOR_MAP_SWIZZLE_NONE)
+        : make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dws, G, brows, G * 2, SCG, BN,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    return dw_ok &&
+           make_map(mdx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dx, G, rows, G * 4, SCG, BM,
                     CU_TENSOR_MAP_SWIZZLE_NONE) &&
            make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
-                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(mdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dwt, ldt, sgrows, ldt * 4, BN, SCG,
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
+                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <bool kQ4, bool kGrouped>
@@ -690,7 +762,7 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, ldt, G, K, q4))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, ldt, K, q4))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
@@ -701,13 +773,14 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
               : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s);
 }
 
-// MoE workspace after the routing tables: a16 [P][K] binary16, dxg [P][G]
-// binary32 (gathered activation rows and scales in expert order) and the
-// transposed scales dwT [E*G][ldt] binary32.
+// MoE workspace after the routing tables: a16 [P][K] binary16 and dxg [P][G]
+// binary32 (gathered activation rows and scales in expert order), and the
+// m-tile table (at most P / 128 + E tiles, 16 bytes each).
 size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E) {
+    (void)N;
     const int64_t G = K / kGroup;
     return align16((size_t)P * K * 2) + align16((size_t)P * G * 4) +
-           align16((size_t)E * G * ldt_of(N) * 4);
+           (size_t)(P / BM + E + 1) * 16;
 }
 
 cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N, int64_t K,
@@ -715,23 +788,22 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
                               int32_t topk, int32_t x_row_mode, const int32_t* perm,
                               const int32_t* offsets, const int32_t* tile_offsets,
                               void* workspace, cudaStream_t s) {
-    const int64_t G = K / kGroup, ldt = ldt_of(N);
+    const int64_t G = K / kGroup;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* a16 = reinterpret_cast<__half*>(ws);
     float* dxg = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2));
-    float* dwt = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2) + align16((size_t)P * G * 4));
+    int4* info = reinterpret_cast<int4*>(ws + align16((size_t)P * K * 2) + align16((size_t)P * G * 4));
     // gather + widen the routed rows (count read on the device: offsets[E])
     widen_rows_kernel<<<widen_grid(P * (K / 16)), 256, 0, s>>>(qx, dx, P, K, a16, dxg, perm,
                                                                offsets + E, topk, x_row_mode);
-    transpose_scales_kernel<<<widen_grid((int64_t)E * ldt * G), 256, 0, s>>>(dw, N, G, E, dwt, ldt);
+    tile_info_kernel<<<(E + 127) / 128, 128, 0, s>>>(offsets, tile_offsets, E, info);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dwt, P, (int64_t)E * N, ldt,
-                   (int64_t)E * G, K, true))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dw, P, (int64_t)E * N, 0, K, true))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
-    GroupedArgs ga{perm, offsets, tile_offsets, E, N};
+    GroupedArgs ga{perm, offsets, tile_offsets, info, E, N};
     dim3 grid((unsigned)sm_count());
     return launch_kernel<true, true>(grid, ma, mb, mdx, mdw, y, P, N, K, N, ga, n_tiles, 0, s);
 }
