@@ -26,12 +26,12 @@ __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
-    "workspace_size",
+    "workspace_size", "debug_group_dots",
     "sm_count", "device_error",
 ]
 
 ALGO_AUTO, ALGO_GEMV, ALGO_MMA, ALGO_TCGEN05 = 0, 1, 2, 3
-OP_QGEMM_Q8_0, OP_QGEMM_Q4_0, OP_GROUPED_MOE = 1, 2, 3
+OP_QGEMM_Q8_0, OP_QGEMM_Q4_0, OP_GROUPED_MOE, OP_DEBUG_GROUP_DOTS = 1, 2, 3, 4
 
 
 def _ptr(t):
@@ -145,6 +145,24 @@ def qgemm_q8_0(qx, dx, qw, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
 def qgemm_q4_0(qx, dx, qw4, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
     """As qgemm_q8_0 with Q4_0 weights qw4 uint8 [N, K/2]."""
     return _dense("qgemm_q4_0_ex", qx, dx, qw4, dw, y, algo, workspace, torch.uint8, 2)
+
+
+def debug_group_dots(qx, qw, bits: int, algo: int = ALGO_AUTO):
+    """Test-only: the exact group dots S int32 [M, N, K/32] as the product kernel
+    `algo` forms them (qw int8 [N, K] for bits 8, uint8 [N, K/2] for bits 4)."""
+    _need(qx, torch.int8, "qx")
+    dev = qx.device
+    _need(qw, torch.int8 if bits == 8 else torch.uint8, "qw", dev)
+    M, K = qx.shape
+    N = qw.shape[0]
+    if qw.shape[1] * (1 if bits == 8 else 2) != K:
+        raise ValueError("shape mismatch between qx and qw")
+    S = torch.empty((M, N, K // 32), dtype=torch.int32, device=dev)
+    nbytes = workspace_size(OP_DEBUG_GROUP_DOTS, M, N, K)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _native.call("qgemm_debug_group_dots", _ptr(qx), M, N, K, _ptr(qw), int(bits), int(algo),
+                 _ptr(S), _ptr(ws), ws.numel(), _stream(dev))
+    return S
 
 
 def moe_route(topk_ids: torch.Tensor, E: int, d_err: torch.Tensor | None = None):

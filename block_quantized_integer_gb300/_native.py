@@ -37,6 +37,8 @@ SIGNATURES = {
                                          P, P, SZ, P]),
     "grouped_qgemm_moe_noalloc": (ctypes.c_int, [P, P, I64, I64, P, I64, I32, I32, P, P, I32,
                                                  I64, P, P, P]),
+    "qgemm_debug_group_dots": (ctypes.c_int, [P, I64, I64, I64, P, ctypes.c_int, ctypes.c_int, P,
+                                              P, SZ, P]),
 }
 
 

@@ -128,6 +128,24 @@ unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 // boxes), else on the warp-MMA kernel.
 bool moe_use_tc(int64_t K) { return K > 0 && K % 256 == 0; }
 
+// Debug group-dot workspace: dx = 1 [M][G] f32 | dw one-hot [N][G] binary16 |
+// y [M][N] f32 | the dense product's workspace (sized for any algo).
+struct DebugWs {
+    size_t dx, dw, y, prod, total;
+};
+DebugWs debug_ws(int64_t M, int64_t N, int64_t K) {
+    DebugWs w{};
+    const int64_t G = K / kGroup;
+    size_t o = 0;
+    w.dx = o;   o = align_up(o + 4 * (size_t)(M * G), 16);
+    w.dw = o;   o = align_up(o + 2 * (size_t)(N * G), 16);
+    w.y = o;    o = align_up(o + 4 * (size_t)(M * N), 16);
+    w.prod = o;
+    if (K % 256 == 0) o += qg::tc_gemm_workspace(M > 9 ? M : 9, N, K);
+    w.total = o;
+    return w;
+}
+
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
                             int32_t E) {
     if (op == QG_OP_GROUPED_MOE) {
@@ -135,6 +153,10 @@ size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, 
         size_t w = moe_ws(T * topk, E).total;
         if (moe_use_tc(K) && N > 0) w += qg::tc_grouped_workspace(T * topk, N, K, E);
         return w;
+    }
+    if (op == QG_OP_DEBUG_GROUP_DOTS) {
+        if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
+        return debug_ws(M, N, K).total;
     }
     if (op == QG_OP_QGEMM_Q8_0 || op == QG_OP_QGEMM_Q4_0) {
         // the tensor-core path widens the activation codes to binary16 first
@@ -249,6 +271,32 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
                                                perm, offsets, tiles, ws + w.total, stream));
     qg::GatherArgs ga{perm, offsets, tiles, E, topk, x_row_mode};
     return from_cuda(qg::launch_mma_grouped(qx, dx, P, N, K, qw4, dw, y, ga, stream));
+}
+
+qg_status qgemm_debug_group_dots(const int8_t* qx, int64_t M, int64_t N, int64_t K,
+                                 const void* qw, int bits, int algo, int32_t* S,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || K % kGroup != 0 || (bits != 8 && bits != 4))
+        return QG_ERR_INVALID_ARG;
+    if (M == 0) return QG_OK;
+    if (!qx || !qw || !S) return QG_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(qw) || ((uintptr_t)S & 3u)) return QG_ERR_ALIGNMENT;
+    const DebugWs w = debug_ws(M, N, K);
+    if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return QG_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* dx = reinterpret_cast<float*>(ws + w.dx);
+    uint16_t* dw = reinterpret_cast<uint16_t*>(ws + w.dw);
+    float* y = reinterpret_cast<float*>(ws + w.y);
+    const int64_t G = K / kGroup;
+    if (qg::launch_fill_ones(dx, M * G, stream) != cudaSuccess) return QG_ERR_CUDA;
+    for (int64_t g = 0; g < G; ++g) {
+        if (qg::launch_one_hot_scales(dw, N, G, g, stream) != cudaSuccess) return QG_ERR_CUDA;
+        const qg_status st = dense(qx, dx, M, N, K, qw, bits == 4, dw, y, N, ws + w.prod,
+                                   w.total - w.prod, algo, stream);
+        if (st != QG_OK) return st;
+        if (qg::launch_scatter_group(y, M, N, G, g, S, stream) != cudaSuccess) return QG_ERR_CUDA;
+    }
+    return QG_OK;
 }
 
 }  // extern "C"

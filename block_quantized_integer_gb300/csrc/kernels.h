@@ -59,4 +59,10 @@ cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, i
                              int32_t* tile_offsets, int bm, float* y, int64_t N,
                              int32_t* d_err, cudaStream_t s);
 
+// Test-only group-dot readout (qgemm_debug_group_dots).
+cudaError_t launch_fill_ones(float* v, int64_t n, cudaStream_t s);
+cudaError_t launch_one_hot_scales(uint16_t* dw, int64_t N, int64_t G, int64_t g, cudaStream_t s);
+cudaError_t launch_scatter_group(const float* y, int64_t M, int64_t N, int64_t G, int64_t g,
+                                 int32_t* S, cudaStream_t s);
+
 }  // namespace qg

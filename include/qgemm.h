@@ -65,7 +65,8 @@ typedef enum {
 } qg_algo;
 
 /* Workspace sizing: op is one of the QG_OP_* values. */
-enum { QG_OP_QGEMM_Q8_0 = 1, QG_OP_QGEMM_Q4_0 = 2, QG_OP_GROUPED_MOE = 3 };
+enum { QG_OP_QGEMM_Q8_0 = 1, QG_OP_QGEMM_Q4_0 = 2, QG_OP_GROUPED_MOE = 3,
+       QG_OP_DEBUG_GROUP_DOTS = 4 };
 
 /* Human-readable name of a status. Never NULL. */
 const char* qg_status_string(qg_status s);
@@ -79,6 +80,23 @@ const char* qg_status_string(qg_status s);
  * (M ignored).  Workspace pointers must be 16-byte aligned. */
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,
                             int64_t T, int32_t topk, int32_t E);
+
+/* Test-only readout of the exact group dot products
+ *   S[m][n][g] = sum_{k = 32g .. 32g+31} qx[m,k] * qw[n,k]
+ * as the dense product kernel `algo` forms them (QG_ALGO_AUTO: the kernel the
+ * product itself would pick).  The kernel runs once per group g with every
+ * activation scale 1 and the weight scales 1 on group g, 0 elsewhere, so its
+ * binary32 output is S of that group exactly (|S| <= 32 * 127^2 < 2^19); the
+ * result is stored as int32.  No counterpart in the pages: it exists so that a
+ * test can compare the integer stage of every kernel bit for bit.
+ *   qw: int8 [N][K] (bits 8) or packed uint8 [N][K/2] (bits 4).
+ *   S:  int32 [M][N][G], device.
+ *   workspace: qgemm_workspace_size(QG_OP_DEBUG_GROUP_DOTS, M, N, K, 0, 0, 0)
+ *   bytes, 16-byte aligned (scale planes, one y plane and the product's own
+ *   workspace).  Runs 3 G + 1 launches on `stream`; slow by design. */
+qg_status qgemm_debug_group_dots(const int8_t* qx, int64_t M, int64_t N, int64_t K,
+                                 const void* qw, int bits, int algo, int32_t* S,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Activation quantization, per row m and 32-group g (Methodology 2 of the MoE
  * page: 8-bit activations; Q8 block rule):

@@ -91,3 +91,18 @@ def test_moe_validation_and_workspace(lib):
     assert g(A, B, 947, 2048, C, 947, 8, 2, D, E, 128, 2048, Y, C, W, ws, S) == 1
     assert g(A, B, 947, 2048, C, 947, 8, 0, D, E, 2000, 2048, Y, C, W, ws, S) == 1  # E > 1024
     assert lib.moe_route(A, 10, 2, 2000, B, C, D, Y, S) == 1
+
+
+def test_debug_group_dots_validation(lib):
+    f = lib.qgemm_debug_group_dots
+    ws = lib.qgemm_workspace_size(4, 16, 64, 512, 0, 0, 0)
+    # dx [16][16] f32 + dw [64][16] f16 + y [16][64] f32 + the tcgen05 workspace for M = 9..16
+    assert ws >= 16 * 16 * 4 + 64 * 16 * 2 + 16 * 64 * 4 and ws % 16 == 0
+    W = ctypes.c_void_p(0x70000)
+    assert f(A, 16, 64, 500, C, 8, 0, Y, W, ws, S) == 1       # K % 32
+    assert f(A, 16, 64, 512, C, 5, 0, Y, W, ws, S) == 1       # bits
+    assert f(A, 16, 64, 512, C, 8, 0, NUL, W, ws, S) == 1     # null S
+    assert f(ctypes.c_void_p(0x10008), 16, 64, 512, C, 8, 0, Y, W, ws, S) == 2
+    assert f(A, 16, 64, 512, C, 8, 0, Y, W, ws - 16, S) == 3  # workspace too small
+    assert f(A, 16, 64, 512, C, 8, 0, Y, NUL, ws, S) == 3
+    assert f(A, 0, 64, 512, C, 8, 0, Y, W, ws, S) == 0        # M == 0: no-op

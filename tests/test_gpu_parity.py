@@ -112,6 +112,32 @@ def test_group_dots_exact(algo, bits):
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("algo,M,N,K", [(qg.ALGO_GEMV, 3, 70, 96), (qg.ALGO_GEMV, 8, 33, 512),
+                                         (qg.ALGO_MMA, 37, 150, 256), (qg.ALGO_TCGEN05, 130, 200, 512),
+                                         (qg.ALGO_AUTO, 9, 129, 256)])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_debug_group_dots_bit_exact(algo, M, N, K, bits):
+    """The C-ABI group-dot readout of each kernel equals the oracle's int64 dots."""
+    rng = np.random.default_rng(1000 + 7 * M + bits + algo)
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    qx[0, :32] = 127
+    qx[-1, -32:] = -127
+    if bits == 8:
+        qw = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        qw[0, :32] = 127
+        qw[-1, -32:] = 127
+    else:
+        qw = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+        qw[0, :16] = 0x00                  # all elements -8
+    S = qg.debug_group_dots(to_dev(qx), to_dev(qw), bits, algo)
+    _sync()
+    ref = oracle.group_dots(qx, qw, K, bits)
+    assert np.array_equal(to_np(S).astype(np.int64), ref)
+    if bits == 8:
+        assert ref[0, 0, 0] == 32 * 127 * 127 and ref[-1, -1, -1] == -32 * 127 * 127
+    assert qg.device_error() == 0
+
+
 # ------------------------------------------------------------------ dense products
 
 def _case(M, N, K, bits, seed):
