@@ -359,6 +359,69 @@ def moe_section(dev, peaks, reps=20):
     return res
 
 
+def moe_layer_section(dev, peaks, reps=20):
+    """The whole MoE layer on the MoE workload: gate/up grouped GEMM -> SwiGLU +
+    re-quantization -> down grouped GEMM (one activation row per pair) ->
+    router-weighted combine, every step through the C ABI on one stream."""
+    import torch
+    import block_quantized_integer_gb300 as qg
+    from block_quantized_integer_gb300 import inputs
+    d = inputs.moe_case()
+    ids = torch.from_numpy(d["topk_ids"]).to(dev)
+    rw = torch.from_numpy(d["route_w"]).to(dev)
+    T, topk = ids.shape
+    P = T * topk
+    w1, w2 = d["w_gate_up"], d["w_down"]
+    E, N1, K1 = w1.shape
+    _, N2, K2 = w2.shape
+    F = N1 // 2
+    q1, d1 = qg.quantize_weight_q4_0(torch.from_numpy(w1.reshape(E * N1, K1)).to(dev))
+    q2, d2 = qg.quantize_weight_q4_0(torch.from_numpy(w2.reshape(E * N2, K2)).to(dev))
+    q1, d1 = q1.view(E, N1, K1 // 2), d1.view(E, N1, K1 // 32)
+    q2, d2 = q2.view(E, N2, K2 // 2), d2.view(E, N2, K2 // 32)
+    qx, dx = qg.quantize_act_q8(torch.from_numpy(d["x_tok"]).to(dev))
+    gu = torch.empty((P, N1), dtype=torch.float32, device=dev)
+    yd = torch.empty((P, N2), dtype=torch.float32, device=dev)
+    out = torch.empty((T, N2), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws1 = torch.empty(qg.workspace_size(qg.OP_GROUPED_MOE, 0, N1, K1, T, topk, E), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(qg.workspace_size(qg.OP_GROUPED_MOE, 0, N2, K2, T, topk, E), dtype=torch.uint8, device=dev)
+    scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def layer(ev=None):
+        if ev: ev[0].record()
+        qg.grouped_qgemm_moe(qx, dx, ids, 0, q1, d1, y=gu, d_err=err, workspace=ws1)
+        if ev: ev[1].record()
+        qh, dh = qg.moe_swiglu_quant(gu, F)
+        if ev: ev[2].record()
+        qg.grouped_qgemm_moe(qh, dh, ids, 1, q2, d2, y=yd, d_err=err, workspace=ws2)
+        if ev: ev[3].record()
+        qg.moe_combine(yd, rw, out=out)
+        if ev: ev[4].record()
+
+    for _ in range(3):
+        layer()
+    steps = {k: [] for k in ("gate_up", "swiglu_quant", "down", "combine", "total")}
+    for _ in range(reps):
+        scrub.fill_(1.0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        layer(ev)
+        torch.cuda.synchronize()
+        t = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+        for k, v in zip(("gate_up", "swiglu_quant", "down", "combine"), t):
+            steps[k].append(v)
+        steps["total"].append(ev[0].elapsed_time(ev[4]))
+    res = {k + "_ms": statistics.median(v) for k, v in steps.items()}
+    wbytes = (np.unique(d["topk_ids"]).size * (N1 * K1 + N2 * K2) * (0.5 + 2 / 32))
+    res["weight_gbs"] = wbytes / (res["total_ms"] * 1e-3) / 1e9
+    res["frac_of_hbm_weights"] = res["weight_gbs"] / peaks["hbm_gbs"]
+    res["workload"] = ("MoE layer: 947 tokens top-8 Zipf(1.1) over 128 experts; gate/up N=2048 K=2048, "
+                       "SwiGLU + int8 re-quantization F=1024, down N=2048 K=1024, router-weighted combine")
+    res["l2"] = "flushed before every timed layer"
+    del scrub
+    return res
+
+
 # --------------------------------------------------------------------------- main
 
 def main():
@@ -368,7 +431,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
-    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "moe_layer", "decode"], default=None,
                     help="run one section only (for profiling); prints its JSON")
     ap.add_argument("--reps", type=int, default=20, help="timed calls per prefill/MoE shape")
     args = ap.parse_args()
@@ -383,6 +446,8 @@ def main():
             out = prefill_section(dev, peaks, reps=args.reps, long_ctx=True)
         elif args.only == "moe":
             out = moe_section(dev, peaks, reps=args.reps)
+        elif args.only == "moe_layer":
+            out = moe_layer_section(dev, peaks, reps=args.reps)
         else:
             projs = make_decode(dev, 1)
             graphs = DecodeGraphs(projs)
@@ -496,6 +561,7 @@ def main():
                                                        long_ctx=True)
         torch.cuda.empty_cache()
         line["moe"] = moe_section(dev, peaks, reps=args.reps)
+        line["moe_layer"] = moe_layer_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
 
     if rank == 0:

@@ -26,6 +26,7 @@ __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
+    "moe_swiglu_quant", "moe_combine",
     "workspace_size", "debug_group_dots",
     "sm_count", "device_error",
 ]
@@ -145,6 +146,38 @@ def qgemm_q8_0(qx, dx, qw, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
 def qgemm_q4_0(qx, dx, qw4, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
     """As qgemm_q8_0 with Q4_0 weights qw4 uint8 [N, K/2]."""
     return _dense("qgemm_q4_0_ex", qx, dx, qw4, dw, y, algo, workspace, torch.uint8, 2)
+
+
+def moe_swiglu_quant(gu: torch.Tensor, F: int | None = None):
+    """gu float32 [P, >= 2F] (gate columns [0, F), up [F, 2F)) ->
+    (qh int8 [P, F], dh float32 [P, F/32]): h = silu(gate) * up quantized per 32-group."""
+    _need(gu, torch.float32, "gu", rows_strided=True)
+    P = gu.shape[0]
+    if F is None:
+        F = gu.shape[1] // 2
+    qh = torch.empty((P, F), dtype=torch.int8, device=gu.device)
+    dh = torch.empty((P, F // 32), dtype=torch.float32, device=gu.device)
+    _native.call("moe_swiglu_quant", _ptr(gu), P, F, gu.stride(0), _ptr(qh), _ptr(dh),
+                 _stream(gu.device))
+    return qh, dh
+
+
+def moe_combine(y: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None):
+    """y float32 [T*topk, N] (token, slot order), w float32 [T, topk] -> out [T, N] =
+    sum over slots of w * y, slot order."""
+    _need(y, torch.float32, "y")
+    dev = y.device
+    _need(w, torch.float32, "w", dev)
+    T, topk = w.shape
+    N = y.shape[1]
+    if y.shape[0] != T * topk:
+        raise ValueError("y must have T * topk rows")
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=dev)
+    else:
+        _need(out, torch.float32, "out", dev)
+    _native.call("moe_combine", _ptr(y), _ptr(w), T, topk, N, _ptr(out), _stream(dev))
+    return out
 
 
 def debug_group_dots(qx, qw, bits: int, algo: int = ALGO_AUTO):

@@ -299,4 +299,22 @@ qg_status qgemm_debug_group_dots(const int8_t* qx, int64_t M, int64_t N, int64_t
     return QG_OK;
 }
 
+qg_status moe_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu, int8_t* qh,
+                           float* dh, cudaStream_t stream) {
+    if (P < 0 || F <= 0 || F % kGroup != 0 || ldgu < 2 * F) return QG_ERR_INVALID_ARG;
+    if (P == 0) return QG_OK;
+    if (!gu || !qh || !dh) return QG_ERR_INVALID_ARG;
+    if (!aligned16(qh) || ((uintptr_t)gu & 3u) || ((uintptr_t)dh & 3u)) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_swiglu_quant(gu, P, F, ldgu, qh, dh, stream));
+}
+
+qg_status moe_combine(const float* y, const float* w, int64_t T, int32_t topk, int64_t N,
+                      float* out, cudaStream_t stream) {
+    if (T < 0 || topk <= 0 || N <= 0) return QG_ERR_INVALID_ARG;
+    if (T == 0) return QG_OK;
+    if (!y || !w || !out) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)y & 3u) || ((uintptr_t)w & 3u) || ((uintptr_t)out & 3u)) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_combine(y, w, T, topk, N, out, stream));
+}
+
 }  // extern "C"

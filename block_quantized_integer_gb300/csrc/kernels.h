@@ -59,6 +59,12 @@ cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, i
                              int32_t* tile_offsets, int bm, float* y, int64_t N,
                              int32_t* d_err, cudaStream_t s);
 
+// MoE steps around the grouped GEMM.
+cudaError_t launch_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu, int8_t* qh,
+                                float* dh, cudaStream_t s);
+cudaError_t launch_combine(const float* y, const float* w, int64_t T, int topk, int64_t N,
+                           float* out, cudaStream_t s);
+
 // Test-only group-dot readout (qgemm_debug_group_dots).
 cudaError_t launch_fill_ones(float* v, int64_t n, cudaStream_t s);
 cudaError_t launch_one_hot_scales(uint16_t* dw, int64_t N, int64_t G, int64_t g, cudaStream_t s);

@@ -1,0 +1,135 @@
+// The MoE steps on either side of the grouped GEMM ("A 35B Hybrid-Attention
+// Mixture-of-Experts Model on a 6GB 2011 GPU", Methodology 1: grouped 4-bit
+// GEMM for MoE routing, 8-bit activations into the W4A8 products;
+// Methodology 2: router-weighted experts):
+//
+//   swiglu_quant: h[p, j] = silu(gate[p, j]) * up[p, j],  silu(v) = v / (1 + e^-v),
+//                 then h re-quantized to int8 codes + binary32 scale per
+//                 32-group with the activation rule (d = max|h| / 127 by one
+//                 IEEE division, q = clamp(round_half_even(h / d), -127, 127)),
+//                 ready to be the activation rows of the down projection;
+//   combine:      out[t, n] = sum_{s < topk} w[t, s] * y[t * topk + s, n], the
+//                 slots summed in order with binary32 FMAs.
+//
+// Both are HBM-bound streaming kernels: swiglu_quant reads 8 bytes and writes
+// 1.125 per output element; combine reads topk * (4 + 4 / N) bytes and writes
+// 4 per output element.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qg {
+
+namespace {
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__device__ __forceinline__ int quant127(float v, float d) {
+    if (d == 0.0f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(v, d));
+    return min(max(q, -127), 127);
+}
+
+// 8 threads per 32-group, 4 consecutive elements (one 16-byte load of gate
+// and one of up) per thread; a warp covers 4 groups.
+__global__ void __launch_bounds__(256)
+swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t ldgu,
+                    int8_t* __restrict__ qh, float* __restrict__ dh, bool vec_ok) {
+    const int64_t G = F / kGroup;
+    const int64_t total = P * G;
+    const int sub = threadIdx.x & 7;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 3);
+    const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
+    const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
+    for (int64_t base = warp_first; base < total; base += stride) {   // whole warps iterate
+        const int64_t grp = base + ((threadIdx.x & 31) >> 3);
+        const bool active = grp < total;
+        const int64_t p = active ? grp / G : 0, g = active ? grp % G : 0;
+        float h[4] = {0.f, 0.f, 0.f, 0.f};
+        if (active) {
+            const float* gp = gu + p * ldgu + g * kGroup + sub * 4;
+            float4 a, b;
+            if (vec_ok) {
+                a = *reinterpret_cast<const float4*>(gp);
+                b = *reinterpret_cast<const float4*>(gp + F);
+            } else {
+                a = make_float4(gp[0], gp[1], gp[2], gp[3]);
+                b = make_float4(gp[F], gp[F + 1], gp[F + 2], gp[F + 3]);
+            }
+            h[0] = silu_mul(a.x, b.x);
+            h[1] = silu_mul(a.y, b.y);
+            h[2] = silu_mul(a.z, b.z);
+            h[3] = silu_mul(a.w, b.w);
+        }
+        float m = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        const float d = __fdiv_rn(m, 127.0f);
+        if (active) {
+            const uint32_t packed = (uint32_t)(quant127(h[0], d) & 0xff) |
+                                    ((uint32_t)(quant127(h[1], d) & 0xff) << 8) |
+                                    ((uint32_t)(quant127(h[2], d) & 0xff) << 16) |
+                                    ((uint32_t)(quant127(h[3], d) & 0xff) << 24);
+            *reinterpret_cast<uint32_t*>(qh + p * F + g * kGroup + sub * 4) = packed;
+            if (sub == 0) dh[p * G + g] = d;
+        }
+    }
+}
+
+// One thread per 4 consecutive outputs of a token row (vec) or per output.
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t T, int topk,
+               int64_t N, float* __restrict__ out, bool vec4) {
+    const int64_t per_row = vec4 ? N / 4 : N;
+    const int64_t total = T * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_row, c = i % per_row;
+        const float* wt = w + t * topk;
+        const float* yt = y + t * topk * N;
+        if (vec4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < topk; ++s) {
+                const float ws = wt[s];
+                const float4 v = *reinterpret_cast<const float4*>(yt + s * N + 4 * c);
+                acc.x = fmaf(ws, v.x, acc.x);
+                acc.y = fmaf(ws, v.y, acc.y);
+                acc.z = fmaf(ws, v.z, acc.z);
+                acc.w = fmaf(ws, v.w, acc.w);
+            }
+            *reinterpret_cast<float4*>(out + t * N + 4 * c) = acc;
+        } else {
+            float acc = 0.f;
+            for (int s = 0; s < topk; ++s) acc = fmaf(wt[s], yt[s * N + c], acc);
+            out[t * N + c] = acc;
+        }
+    }
+}
+
+int stream_grid(int64_t work) {
+    int64_t b = (work + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu, int8_t* qh,
+                                float* dh, cudaStream_t s) {
+    const bool vec_ok = ((uintptr_t)gu % 16 == 0) && (ldgu % 4 == 0) && (F % 4 == 0);
+    const int64_t threads = P * (F / kGroup) * 8;
+    swiglu_quant_kernel<<<stream_grid(threads), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* y, const float* w, int64_t T, int topk, int64_t N,
+                           float* out, cudaStream_t s) {
+    const bool vec4 = (N % 4 == 0) && ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
+    combine_kernel<<<stream_grid(T * (vec4 ? N / 4 : N)), 256, 0, s>>>(y, w, T, topk, N, out, vec4);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -120,7 +120,9 @@ def moe_case(E: int = MOE_EXPERTS, T: int = MOE_TOKENS, topk: int = MOE_TOPK,
     """Expert weights, token activations and routing of the MoE workload.
 
     Returns dict with w_gate_up [E,N1,K1], w_down [E,N2,K2] (fp32), x_tok [T,K1],
-    x_pair [T*topk,K2] (fp32) and topk_ids [T,topk] int32."""
+    x_pair [T*topk,K2] (fp32), topk_ids [T,topk] int32 and route_w [T,topk] fp32
+    (router weights of each token's slots, positive, summing to one; drawn last so
+    the other arrays do not depend on them)."""
     rng = rng_for(MOE, sub)
     N1, K1 = gate_up
     N2, K2 = down
@@ -129,4 +131,6 @@ def moe_case(E: int = MOE_EXPERTS, T: int = MOE_TOKENS, topk: int = MOE_TOPK,
     x_tok = normal(rng, (T, K1))
     x_pair = normal(rng, (T * topk, K2))
     ids = zipf_routing(rng, T, E, topk)
-    return dict(w_gate_up=w1, w_down=w2, x_tok=x_tok, x_pair=x_pair, topk_ids=ids)
+    rw = rng.random((T, topk)) + 0.05
+    rw = (rw / rw.sum(axis=1, keepdims=True)).astype(np.float32)
+    return dict(w_gate_up=w1, w_down=w2, x_tok=x_tok, x_pair=x_pair, topk_ids=ids, route_w=rw)

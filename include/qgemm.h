@@ -174,6 +174,29 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
                             int32_t E, int64_t N, float* y, int32_t* d_err,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* SwiGLU between the MoE gate/up and down products, re-quantized for the
+ * down product (Methodology 1 of the MoE page: 8-bit activations into the
+ * W4A8 grouped GEMM; the pages do not spell the activation out, the usual
+ * gated one is taken):
+ *   h[p, j] = silu(gu[p, j]) * gu[p, F + j],  silu(v) = v / (1 + exp(-v)),
+ * evaluated in binary32 (expf, IEEE division and products), then per row p
+ * and 32-group the activation rule of quantize_act_q8.
+ *   gu: float32 [P][ldgu], ldgu >= 2F, gate in columns [0, F), up in [F, 2F)
+ *       (the fused gate/up output of grouped_qgemm_moe);
+ *   qh: int8 [P][F] (16-byte aligned), dh: float32 [P][F/32].  F % 32 == 0.
+ * Codes agree with a binary64 evaluation of h except where h / d lies within
+ * a few binary32 rounding errors of a half-integer. */
+qg_status moe_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu,
+                           int8_t* qh, float* dh, cudaStream_t stream);
+
+/* Router-weighted combine of the routed rows back into token rows:
+ *   out[t][n] = sum_{s = 0 .. topk-1} w[t][s] * y[t * topk + s][n],
+ * summed in slot order with binary32 FMAs (deterministic).  y float32
+ * [T*topk][N] in (token, slot) order (the down output of grouped_qgemm_moe;
+ * unrouted pairs hold zero rows), w float32 [T][topk], out float32 [T][N]. */
+qg_status moe_combine(const float* y, const float* w, int64_t T, int32_t topk, int64_t N,
+                      float* out, cudaStream_t stream);
+
 /* grouped_qgemm_moe for callers that cannot allocate device memory: same
  * arguments, results and errors as grouped_qgemm_moe, minus the workspace.
  * (No counterpart in the pages this library follows: it exists for callers

@@ -64,6 +64,8 @@ def _L():
             lib.orc_moe_route.argtypes = [P, I64, I32, I32, P, P, P]
             lib.orc_grouped_qgemm_moe.restype = I64
             lib.orc_grouped_qgemm_moe.argtypes = [P, P, I64, P, I64, I32, I32, P, P, I32, I64, P, P]
+            lib.orc_silu_mul.argtypes = [P, I64, I64, I64, P]
+            lib.orc_moe_combine.argtypes = [P, P, I64, I32, I64, P, P]
             _lib = lib
     return _lib
 
@@ -195,3 +197,25 @@ def grouped_qgemm_moe(qx, dx, topk_ids, x_row_mode: int, qw4, dw):
     bad = _L().orc_grouped_qgemm_moe(_p(qx), _p(dx), K, _p(ids), T, topk, x_row_mode,
                                      _p(qw4), _p(dw), E, N, _p(y), _p(mag))
     return y, mag, int(bad)
+
+
+def silu_mul(gu: np.ndarray, F: int) -> np.ndarray:
+    """h [P, F] binary64 = silu(gu[:, :F]) * gu[:, F:2F] (gu binary32 [P, >= 2F])."""
+    gu = _c(gu, np.float32)
+    P, ld = gu.shape
+    h = np.empty((P, F), np.float64)
+    _L().orc_silu_mul(_p(gu), P, F, ld, _p(h))
+    return h
+
+
+def moe_combine(y: np.ndarray, w: np.ndarray):
+    """(out [T, N] binary64, mag [T, N]) = router-weighted sum of the topk rows of each token."""
+    y = _c(y, np.float32)
+    w = _c(w, np.float32)
+    T, topk = w.shape
+    N = y.shape[1]
+    out = np.empty((T, N), np.float64)
+    mag = np.empty((T, N), np.float64)
+    _L().orc_moe_combine(_p(y), _p(w), T, topk, N, _p(out), _p(mag))
+    return out, mag
+

@@ -299,3 +299,34 @@ int64_t orc_grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t K,
     }
     return bad;
 }
+
+/* The MoE steps around the grouped product (readings where the pages are
+ * silent: the usual gated expert activation, and a router-weighted sum of
+ * the expert rows of each token).
+ *
+ * h[p][j] = silu(gate) * up with silu(v) = v / (1 + exp(-v)), in binary64,
+ * gate = gu[p][j], up = gu[p][F + j]; gu is binary32 [P][ldgu]. */
+void orc_silu_mul(const float* gu, int64_t P, int64_t F, int64_t ldgu, double* h) {
+    for (int64_t p = 0; p < P; ++p)
+        for (int64_t j = 0; j < F; ++j) {
+            double g = (double)gu[p * ldgu + j], u = (double)gu[p * ldgu + F + j];
+            h[p * F + j] = g / (1.0 + exp(-g)) * u;
+        }
+}
+
+/* out[t][n] = sum_s w[t][s] * y[t * topk + s][n] in binary64, slot order;
+ * mag[t][n] = sum_s |w[t][s] * y[t * topk + s][n]|. */
+void orc_moe_combine(const float* y, const float* w, int64_t T, int32_t topk, int64_t N,
+                     double* out, double* mag) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, m = 0.0;
+            for (int32_t s = 0; s < topk; ++s) {
+                double v = (double)w[t * topk + s] * (double)y[(t * topk + s) * N + n];
+                acc += v;
+                m += fabs(v);
+            }
+            out[t * N + n] = acc;
+            mag[t * N + n] = m;
+        }
+}

@@ -106,3 +106,19 @@ def test_debug_group_dots_validation(lib):
     assert f(A, 16, 64, 512, C, 8, 0, Y, W, ws - 16, S) == 3  # workspace too small
     assert f(A, 16, 64, 512, C, 8, 0, Y, NUL, ws, S) == 3
     assert f(A, 0, 64, 512, C, 8, 0, Y, W, ws, S) == 0        # M == 0: no-op
+
+
+def test_moe_ffn_steps_validation(lib):
+    f = lib.moe_swiglu_quant
+    assert f(A, 4, 48, 96, B, C, S) == 1            # F % 32
+    assert f(A, 4, 64, 100, B, C, S) == 1           # ldgu < 2F
+    assert f(A, -1, 64, 128, B, C, S) == 1
+    assert f(A, 0, 64, 128, B, C, S) == 0           # P == 0: no-op
+    assert f(NUL, 4, 64, 128, B, C, S) == 1
+    assert f(A, 4, 64, 128, ctypes.c_void_p(0x20004), C, S) == 2   # qh not 16-byte aligned
+    g = lib.moe_combine
+    assert g(A, B, 4, 0, 64, C, S) == 1             # topk
+    assert g(A, B, 4, 8, 0, C, S) == 1              # N
+    assert g(A, B, 0, 8, 64, C, S) == 0             # T == 0: no-op
+    assert g(A, NUL, 4, 8, 64, C, S) == 1
+    assert g(A, B, 4, 8, 64, ctypes.c_void_p(0x30002), S) == 2

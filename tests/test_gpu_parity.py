@@ -405,3 +405,96 @@ def test_grouped_moe_full_config_sampled(moe_full, which):
         qx_ref, dx_ref = oracle.quantize_act_q8(x[xr])
         y_ref, mag = oracle.qgemm(qx_ref, dx_ref, q_ref, d_ref, 4)
         assert_close(yg[sel], y_ref, mag)
+
+
+# ------------------------------------------------------------------ MoE steps around the GEMM
+
+def _swiglu_reference_check(gu: np.ndarray, F: int, qh: np.ndarray, dh: np.ndarray):
+    """qh/dh against the binary64 SwiGLU: scales within binary32 rounding, codes the
+    round-half-even of h / d except within 1e-4 of a half-integer, where either
+    neighbour is a correct result of a binary32 evaluation."""
+    h = oracle.silu_mul(gu, F)
+    P = h.shape[0]
+    hg = h.reshape(P, F // 32, 32)
+    d_ref = np.abs(hg).max(axis=2) / 127.0
+    assert np.allclose(dh, d_ref, rtol=1e-6, atol=0.0)
+    zero = d_ref == 0
+    assert np.all(dh[zero] == 0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(zero[:, :, None], 0.0, hg / d_ref[:, :, None])
+    q_ref = np.clip(np.rint(r), -127, 127)
+    frac = np.abs(np.abs(r) - np.floor(np.abs(r)) - 0.5)
+    near = frac < 1e-4
+    qg_ = qh.reshape(P, F // 32, 32).astype(np.float64)
+    assert np.array_equal(qg_[~near], q_ref[~near])
+    assert np.all(np.abs(qg_[near] - r[near]) <= 0.5 + 1e-4)
+    return int(near.sum())
+
+
+@pytest.mark.parametrize("P,F,pad", [(300, 1024, 0), (37, 96, 40), (1, 32, 0)])
+def test_swiglu_quant_vs_oracle(P, F, pad):
+    rng = np.random.default_rng(7 + P + F)
+    gu = (rng.standard_normal((P, 2 * F + pad)) * 2.0).astype(np.float32)
+    gu[0, :32] = 0.0                                   # gate 0: h = 0, d = 0, q = 0
+    if P > 1:
+        gu[-1, :4] = [40.0, -40.0, 88.0, -88.0]        # saturated and vanishing gates
+    gu_t = to_dev(gu)
+    qh, dh = qg.moe_swiglu_quant(gu_t, F)
+    _sync()
+    _swiglu_reference_check(gu, F, to_np(qh), to_np(dh))
+    assert np.all(to_np(qh)[0, :32] == 0) and to_np(dh)[0, 0] == 0.0
+
+
+@pytest.mark.parametrize("T,topk,N", [(947, 8, 2048), (13, 3, 1030), (1, 1, 4)])
+def test_moe_combine_vs_oracle(T, topk, N):
+    rng = np.random.default_rng(11 + T + N)
+    y = rng.standard_normal((T * topk, N)).astype(np.float32)
+    y[0] = 0.0                                         # an unrouted pair's zero row
+    w = rng.random((T, topk)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    out = qg.moe_combine(to_dev(y), to_dev(w))
+    _sync()
+    ref, mag = oracle.moe_combine(y, w)
+    err = np.abs(to_np(out).astype(np.float64) - ref)
+    assert np.all(err <= 1e-6 * mag + 1e-30)
+    out2 = qg.moe_combine(to_dev(y), to_dev(w))         # deterministic slot order
+    _sync()
+    assert torch.equal(out, out2)
+
+
+def test_moe_layer_end_to_end():
+    """gate/up -> SwiGLU + re-quantization -> down -> router-weighted combine, all on the
+    GPU through the C ABI, against the oracle's composition of the same steps."""
+    E, T, topk, F, K = 16, 96, 4, 256, 256
+    rng = np.random.default_rng(2026)
+    wgu = (rng.standard_normal((E, 2 * F, K)) * 0.02).astype(np.float32)
+    wdn = (rng.standard_normal((E, K, F)) * 0.02).astype(np.float32)
+    qgu = np.empty((E, 2 * F, K // 2), np.uint8)
+    dgu = np.empty((E, 2 * F, K // 32), np.uint16)
+    qdn = np.empty((E, K, F // 2), np.uint8)
+    ddn = np.empty((E, K, F // 32), np.uint16)
+    for e in range(E):
+        qgu[e], dgu[e] = oracle.quantize_w_q4_0(wgu[e])
+        qdn[e], ddn[e] = oracle.quantize_w_q4_0(wdn[e])
+    ids = inputs.zipf_routing(rng, T, E, topk)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    w = rng.random((T, topk)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    qx, dx = oracle.quantize_act_q8(x)
+    # oracle composition
+    gu_ref, _, _ = oracle.grouped_qgemm_moe(qx, dx, ids, 0, qgu, dgu)
+    qh_ref, dh_ref = oracle.quantize_act_q8(oracle.silu_mul(gu_ref, F).astype(np.float32))
+    yd_ref, yd_mag, _ = oracle.grouped_qgemm_moe(qh_ref, dh_ref, ids, 1, qdn, ddn)
+    out_ref, out_mag = oracle.moe_combine(yd_ref, w)
+    # GPU
+    gu, _ = qg.grouped_qgemm_moe(to_dev(qx), to_dev(dx), to_dev(ids), 0, to_dev(qgu), to_dev(dgu))
+    qh, dh = qg.moe_swiglu_quant(gu, F)
+    yd, _ = qg.grouped_qgemm_moe(qh, dh, to_dev(ids), 1, to_dev(qdn), to_dev(ddn))
+    out = qg.moe_combine(yd, to_dev(w))
+    _sync()
+    flips = int((to_np(qh) != qh_ref).sum())
+    assert flips <= qh_ref.size // 1000            # codes differ only at near-ties
+    # a flipped code moves one down-projection term by one quantum of its row
+    wsum = np.abs(w[:, :, None].astype(np.float64) * yd_mag.reshape(T, topk, K)).sum(1)
+    err = np.abs(to_np(out).astype(np.float64) - out_ref)
+    assert np.all(err <= 1e-5 * wsum + 1e-4 * wsum * (flips > 0) + 1e-30)

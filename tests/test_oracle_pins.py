@@ -392,3 +392,62 @@ def test_moe_unrouted_rows_are_zero():
     y, _, bad = oracle.grouped_qgemm_moe(qx, dx, ids, 0, qw4, dw)
     assert bad == 2
     assert np.all(y[2 * 3 + 1] == 0) and np.all(y[5 * 3 + 0] == 0)
+
+
+# ---------------------------------------------------------------- MoE steps around the GEMM
+
+def test_silu_mul_closed_forms():
+    """silu(0) = 0; sigmoid(1) = e / (1 + e); silu(v) - silu(-v) = v; silu(v) -> v and
+    silu(-v) -> 0 for large v; up scales h linearly."""
+    g = np.array([0.0, 1.0, -1.0, 3.0, -3.0, 40.0, -40.0, 0.5], np.float32)
+    up = np.ones_like(g)
+    gu = np.concatenate([g, up])[None, :]
+    h = oracle.silu_mul(gu, g.size)[0]
+    assert h[0] == 0.0
+    e = np.e
+    assert abs(h[1] - e / (1.0 + e)) < 1e-15
+    assert abs((h[1] - h[2]) - 1.0) < 1e-15                  # silu(1) - silu(-1) = 1
+    assert abs((h[3] - h[4]) - 3.0) < 1e-14
+    assert abs(h[5] - 40.0) < 1e-12 and 0.0 > h[6] > -1e-15
+    gu2 = np.concatenate([g, np.full_like(g, -2.5)])[None, :]
+    h2 = oracle.silu_mul(gu2, g.size)[0]
+    assert np.allclose(h2, -2.5 * h, rtol=1e-15, atol=0.0)
+
+
+def test_silu_mul_layout_gate_then_up():
+    """Columns [0, F) are the gate and [F, 2F) the up half; extra columns are ignored."""
+    rng = np.random.default_rng(41)
+    P, F = 3, 64
+    gu = rng.standard_normal((P, 2 * F + 5)).astype(np.float32)
+    h = oracle.silu_mul(gu, F)
+    g64, u64 = gu[:, :F].astype(np.float64), gu[:, F:2 * F].astype(np.float64)
+    # sigmoid from tanh: 1 / (1 + e^-v) = (1 + tanh(v / 2)) / 2
+    ref = g64 * (1.0 + np.tanh(g64 / 2.0)) / 2.0 * u64
+    assert np.allclose(h, ref, rtol=1e-14, atol=1e-300)
+
+
+def test_moe_combine_pins():
+    """One-hot weights select a slot's row; rows equal and weights summing to one give the
+    row; permuting slots together with their weights changes nothing; mag = sum |w y|."""
+    rng = np.random.default_rng(43)
+    T, topk, N = 5, 4, 24
+    y = rng.standard_normal((T * topk, N)).astype(np.float32)
+    w = np.zeros((T, topk), np.float32)
+    w[np.arange(T), np.arange(T) % topk] = 1.0
+    out, mag = oracle.moe_combine(y, w)
+    for t in range(T):
+        assert np.array_equal(out[t], y[t * topk + t % topk].astype(np.float64))
+    assert np.array_equal(mag, np.abs(out))
+    yc = np.repeat(rng.standard_normal((T, 1, N)), topk, axis=1).reshape(T * topk, N).astype(np.float32)
+    wq = np.full((T, topk), 0.25, np.float32)
+    out_c, _ = oracle.moe_combine(yc, wq)
+    assert np.allclose(out_c, yc[::topk].astype(np.float64), rtol=1e-15, atol=0)
+    wr = rng.random((T, topk)).astype(np.float32)
+    perm = rng.permutation(topk)
+    out1, mag1 = oracle.moe_combine(y, wr)
+    y_p = y.reshape(T, topk, N)[:, perm].reshape(T * topk, N)
+    out2, mag2 = oracle.moe_combine(y_p, wr[:, perm])
+    assert np.allclose(out1, out2, rtol=1e-14, atol=1e-14)
+    assert np.allclose(mag1, mag2, rtol=1e-14, atol=0)
+    assert np.allclose(mag1, np.abs(wr[:, :, None].astype(np.float64) *
+                                    y.reshape(T, topk, N).astype(np.float64)).sum(1), rtol=1e-14)
