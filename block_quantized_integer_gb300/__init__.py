@@ -26,6 +26,7 @@ __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
+    "import_gguf_q8_0", "import_gguf_q4_0",
     "moe_swiglu_quant", "moe_combine",
     "workspace_size", "debug_group_dots",
     "sm_count", "device_error",
@@ -146,6 +147,27 @@ def qgemm_q8_0(qx, dx, qw, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
 def qgemm_q4_0(qx, dx, qw4, dw, y=None, algo: int = ALGO_AUTO, workspace=None):
     """As qgemm_q8_0 with Q4_0 weights qw4 uint8 [N, K/2]."""
     return _dense("qgemm_q4_0_ex", qx, dx, qw4, dw, y, algo, workspace, torch.uint8, 2)
+
+
+def _import_gguf(name, blocks, N, K, bytes_per_block, code_dtype, code_cols):
+    _need(blocks, torch.uint8, "blocks")
+    if blocks.numel() != N * (K // 32) * bytes_per_block:
+        raise ValueError(f"blocks must hold N * K/32 blocks of {bytes_per_block} bytes")
+    dev = blocks.device
+    q = torch.empty((N, code_cols), dtype=code_dtype, device=dev)
+    dw = torch.empty((N, K // 32), dtype=torch.float16, device=dev)
+    _native.call(name, _ptr(blocks), N, K, _ptr(q), _ptr(dw), _stream(dev))
+    return q, dw
+
+
+def import_gguf_q8_0(blocks: torch.Tensor, N: int, K: int):
+    """GGUF Q8_0 blocks (uint8, N * K/32 * 34 bytes) -> (qw int8 [N, K], dw float16 [N, K/32])."""
+    return _import_gguf("import_gguf_q8_0", blocks, N, K, 34, torch.int8, K)
+
+
+def import_gguf_q4_0(blocks: torch.Tensor, N: int, K: int):
+    """GGUF Q4_0 blocks (uint8, N * K/32 * 18 bytes) -> (qw4 uint8 [N, K/2], dw float16 [N, K/32])."""
+    return _import_gguf("import_gguf_q4_0", blocks, N, K, 18, torch.uint8, K // 2)
 
 
 def moe_swiglu_quant(gu: torch.Tensor, F: int | None = None):

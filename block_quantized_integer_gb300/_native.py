@@ -39,6 +39,8 @@ SIGNATURES = {
                                                  I64, P, P, P]),
     "qgemm_debug_group_dots": (ctypes.c_int, [P, I64, I64, I64, P, ctypes.c_int, ctypes.c_int, P,
                                               P, SZ, P]),
+    "import_gguf_q8_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
+    "import_gguf_q4_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
     "moe_swiglu_quant": (ctypes.c_int, [P, I64, I64, I64, P, P, P]),
     "moe_combine": (ctypes.c_int, [P, P, I64, I32, I64, P, P]),
 }

@@ -317,4 +317,23 @@ qg_status moe_combine(const float* y, const float* w, int64_t T, int32_t topk, i
     return from_cuda(qg::launch_combine(y, w, T, topk, N, out, stream));
 }
 
+static qg_status import_gguf(const uint8_t* blocks, int64_t N, int64_t K, void* q, uint16_t* dw,
+                             bool q4, cudaStream_t stream) {
+    if (N < 0 || K <= 0 || K % kGroup != 0) return QG_ERR_INVALID_ARG;
+    if (N == 0) return QG_OK;
+    if (!blocks || !q || !dw) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)blocks & 1u) || !aligned16(q) || ((uintptr_t)dw & 1u)) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_gguf_import(blocks, N, K, q, dw, q4, stream));
+}
+
+qg_status import_gguf_q8_0(const uint8_t* blocks, int64_t N, int64_t K, int8_t* qw, uint16_t* dw,
+                           cudaStream_t stream) {
+    return import_gguf(blocks, N, K, qw, dw, false, stream);
+}
+
+qg_status import_gguf_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* qw4,
+                           uint16_t* dw, cudaStream_t stream) {
+    return import_gguf(blocks, N, K, qw4, dw, true, stream);
+}
+
 }  // extern "C"

@@ -65,6 +65,10 @@ cudaError_t launch_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t l
 cudaError_t launch_combine(const float* y, const float* w, int64_t T, int topk, int64_t N,
                            float* out, cudaStream_t s);
 
+// GGUF interleaved Q8_0 / Q4_0 blocks -> planar codes + binary16 scales.
+cudaError_t launch_gguf_import(const uint8_t* blocks, int64_t N, int64_t K, void* q, uint16_t* d,
+                               bool q4, cudaStream_t s);
+
 // Test-only group-dot readout (qgemm_debug_group_dots).
 cudaError_t launch_fill_ones(float* v, int64_t n, cudaStream_t s);
 cudaError_t launch_one_hot_scales(uint16_t* dw, int64_t N, int64_t G, int64_t g, cudaStream_t s);

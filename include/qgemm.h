@@ -121,6 +121,21 @@ qg_status quantize_weight_q8_0(const float* w, int64_t N, int64_t K,
 qg_status quantize_weight_q4_0(const float* w, int64_t N, int64_t K,
                                uint8_t* qw4, uint16_t* dw, cudaStream_t stream);
 
+/* Import of weights stored as GGUF-style interleaved blocks (the mining-card
+ * page runs the same Q8_0 GGUF files as llama.cpp; the block layout is the
+ * GGUF format's): per 32 weights of a row, a binary16 scale followed by the
+ * codes -- Q8_0: 2 + 32 bytes of int8; Q4_0: 2 + 16 bytes of nibbles in the
+ * qw4 order above -- the K/32 blocks of a row back to back, rows back to back.
+ *   blocks: device, [N][K/32][34] (Q8_0) or [N][K/32][18] (Q4_0), 2-byte
+ *           aligned;
+ *   out:    qw int8 [N][K] / qw4 uint8 [N][K/2] (16-byte aligned), dw
+ *           binary16 bits [N][K/32].
+ * A pure byte move: the codes and scales come out as stored. */
+qg_status import_gguf_q8_0(const uint8_t* blocks, int64_t N, int64_t K, int8_t* qw,
+                           uint16_t* dw, cudaStream_t stream);
+qg_status import_gguf_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* qw4,
+                           uint16_t* dw, cudaStream_t stream);
+
 /* Dense Q8_0 x Q8 product (prefill GEMM for large M, decode GEMV for M <= 8):
  * y = sum_g dw * dx * S as above, every S formed exactly before it is scaled,
  * the sum over groups in binary32 (order depends on the kernel; fixed for a

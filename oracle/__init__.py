@@ -65,6 +65,7 @@ def _L():
             lib.orc_grouped_qgemm_moe.restype = I64
             lib.orc_grouped_qgemm_moe.argtypes = [P, P, I64, P, I64, I32, I32, P, P, I32, I64, P, P]
             lib.orc_silu_mul.argtypes = [P, I64, I64, I64, P]
+            lib.orc_import_gguf.argtypes = [P, I64, I64, ctypes.c_int, P, P]
             lib.orc_moe_combine.argtypes = [P, P, I64, I32, I64, P, P]
             _lib = lib
     return _lib
@@ -218,4 +219,14 @@ def moe_combine(y: np.ndarray, w: np.ndarray):
     mag = np.empty((T, N), np.float64)
     _L().orc_moe_combine(_p(y), _p(w), T, topk, N, _p(out), _p(mag))
     return out, mag
+
+
+def import_gguf(blocks: np.ndarray, N: int, K: int, wbits: int):
+    """GGUF Q8_0 (wbits 8) / Q4_0 (wbits 4) blocks -> (codes [N, K] int8 or [N, K/2] uint8,
+    scales [N, K/32] uint16)."""
+    blocks = _c(blocks, np.uint8)
+    q = np.empty((N, K if wbits == 8 else K // 2), np.int8 if wbits == 8 else np.uint8)
+    d = np.empty((N, K // 32), np.uint16)
+    _L().orc_import_gguf(_p(blocks), N, K, 1 if wbits == 4 else 0, _p(q), _p(d))
+    return q, d
 

@@ -330,3 +330,19 @@ void orc_moe_combine(const float* y, const float* w, int64_t T, int32_t topk, in
             mag[t * N + n] = m;
         }
 }
+
+/* GGUF-style interleaved blocks -> planar codes and binary16 scales (the file
+ * format the mining-card page's engine reads: per 32 weights a little-endian
+ * binary16 scale, then 32 int8 codes (Q8_0) or 16 bytes of nibbles (Q4_0, the
+ * same nibble order as the planar qw4)). */
+void orc_import_gguf(const uint8_t* blocks, int64_t N, int64_t K, int q4, uint8_t* q,
+                     uint16_t* d) {
+    int64_t G = K / ORC_GROUP, block_bytes = q4 ? 18 : 34, code_bytes = q4 ? 16 : 32;
+    int64_t row_bytes = q4 ? K / 2 : K;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < G; ++g) {
+            const uint8_t* b = blocks + (n * G + g) * block_bytes;
+            d[n * G + g] = (uint16_t)(b[0] | (b[1] << 8));
+            memcpy(q + n * row_bytes + g * code_bytes, b + 2, (size_t)code_bytes);
+        }
+}

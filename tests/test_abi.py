@@ -122,3 +122,13 @@ def test_moe_ffn_steps_validation(lib):
     assert g(A, B, 0, 8, 64, C, S) == 0             # T == 0: no-op
     assert g(A, NUL, 4, 8, 64, C, S) == 1
     assert g(A, B, 4, 8, 64, ctypes.c_void_p(0x30002), S) == 2
+
+
+def test_gguf_import_validation(lib):
+    f = lib.import_gguf_q8_0
+    assert f(A, 4, 48, B, C, S) == 1                 # K % 32
+    assert f(A, -1, 64, B, C, S) == 1
+    assert f(A, 0, 64, B, C, S) == 0                 # N == 0: no-op
+    assert f(NUL, 4, 64, B, C, S) == 1
+    assert f(ctypes.c_void_p(0x10001), 4, 64, B, C, S) == 2     # blocks 2-byte aligned
+    assert lib.import_gguf_q4_0(A, 4, 64, ctypes.c_void_p(0x20008), C, S) == 2

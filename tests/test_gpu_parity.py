@@ -498,3 +498,27 @@ def test_moe_layer_end_to_end():
     wsum = np.abs(w[:, :, None].astype(np.float64) * yd_mag.reshape(T, topk, K)).sum(1)
     err = np.abs(to_np(out).astype(np.float64) - out_ref)
     assert np.all(err <= 1e-5 * wsum + 1e-4 * wsum * (flips > 0) + 1e-30)
+
+
+# ------------------------------------------------------------------ GGUF block import
+
+@pytest.mark.parametrize("wbits", [8, 4])
+@pytest.mark.parametrize("N,K", [(37, 96), (300, 4096)])
+def test_gguf_import_bit_exact(wbits, N, K):
+    """The CUDA import equals the oracle byte for byte, and the imported weights give
+    the same product as the same weights quantized planar."""
+    rng = np.random.default_rng(90 + N + wbits)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    q, d = oracle.quantize_w_q8_0(w) if wbits == 8 else oracle.quantize_w_q4_0(w)
+    cb = 32 if wbits == 8 else 16
+    G = K // 32
+    blocks = np.empty((N, G, 2 + cb), np.uint8)
+    blocks[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    blocks[:, :, 1] = (d >> 8).astype(np.uint8)
+    blocks[:, :, 2:] = q.view(np.uint8).reshape(N, G, cb)
+    imp = qg.import_gguf_q8_0 if wbits == 8 else qg.import_gguf_q4_0
+    qt, dt = imp(to_dev(blocks.reshape(-1)), N, K)
+    _sync()
+    q_ref, d_ref = oracle.import_gguf(blocks.reshape(-1), N, K, wbits)
+    assert np.array_equal(to_np(qt).view(np.uint8), q_ref.view(np.uint8))
+    assert np.array_equal(to_np(dt).view(np.uint16), d_ref)

@@ -451,3 +451,56 @@ def test_moe_combine_pins():
     assert np.allclose(mag1, mag2, rtol=1e-14, atol=0)
     assert np.allclose(mag1, np.abs(wr[:, :, None].astype(np.float64) *
                                     y.reshape(T, topk, N).astype(np.float64)).sum(1), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- GGUF block import
+
+def _golden_gguf():
+    vals = {}
+    for line in open(os.path.join(GOLD, "gguf_blocks.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, *rest = line.split()
+        vals[key] = rest
+    return vals
+
+
+def test_gguf_import_golden_blocks():
+    g = _golden_gguf()
+    q8 = np.array([int(b, 16) for b in g["q8_bytes"]], np.uint8)
+    q, d = oracle.import_gguf(q8, 1, 32, 8)
+    assert d[0, 0] == int(g["q8_scale"][0], 16)
+    assert np.array_equal(q[0], np.array([int(v) for v in g["q8_values"]], np.int8))
+    q4 = np.array([int(b, 16) for b in g["q4_bytes"]], np.uint8)
+    q4c, d4 = oracle.import_gguf(q4, 1, 32, 4)
+    assert d4[0, 0] == int(g["q4_scale"][0], 16)
+    # unpack the planar nibbles with the header's rule (byte j: element j low, j+16 high)
+    b = [int(v) for v in q4c[0]]
+    vals = [(b[j] & 15) - 8 for j in range(16)] + [(b[j] >> 4) - 8 for j in range(16)]
+    assert vals == [int(v) for v in g["q4_values"]]
+
+
+def _encode_gguf(q, d, wbits):
+    """Independent writer of the GGUF block layout with struct (little-endian)."""
+    import struct
+    N, G = d.shape
+    cb = 32 if wbits == 8 else 16
+    out = bytearray()
+    for n in range(N):
+        for g in range(G):
+            out += struct.pack("<H", int(d[n, g]))
+            out += q[n, g * cb:(g + 1) * cb].astype(np.uint8).tobytes()
+    return np.frombuffer(bytes(out), np.uint8)
+
+
+@pytest.mark.parametrize("wbits", [8, 4])
+def test_gguf_import_round_trip(wbits):
+    """Quantize planar, write GGUF blocks independently, import: the planes come back."""
+    rng = np.random.default_rng(5 + wbits)
+    N, K = 7, 256
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    q, d = oracle.quantize_w_q8_0(w) if wbits == 8 else oracle.quantize_w_q4_0(w)
+    blocks = _encode_gguf(q, d, wbits)
+    assert blocks.size == N * (K // 32) * (34 if wbits == 8 else 18)
+    q2, d2 = oracle.import_gguf(blocks, N, K, wbits)
+    assert np.array_equal(q2.view(np.uint8), q.view(np.uint8)) and np.array_equal(d2, d)
