@@ -27,6 +27,7 @@ __all__ = [
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
     "import_gguf_q8_0", "import_gguf_q4_0",
+    "attn_splitk_merge",
     "moe_swiglu_quant", "moe_combine",
     "workspace_size", "debug_group_dots",
     "sm_count", "device_error",
@@ -168,6 +169,24 @@ def import_gguf_q8_0(blocks: torch.Tensor, N: int, K: int):
 def import_gguf_q4_0(blocks: torch.Tensor, N: int, K: int):
     """GGUF Q4_0 blocks (uint8, N * K/32 * 18 bytes) -> (qw4 uint8 [N, K/2], dw float16 [N, K/32])."""
     return _import_gguf("import_gguf_q4_0", blocks, N, K, 18, torch.uint8, K // 2)
+
+
+def attn_splitk_merge(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, want_lse: bool = True):
+    """Split-K attention partials m, l float32 [S, R], acc float32 [S, R, D] ->
+    (out float32 [R, D], lse float32 [R] or None), splits merged in index order."""
+    _need(m, torch.float32, "m")
+    dev = m.device
+    _need(l, torch.float32, "l", dev)
+    _need(acc, torch.float32, "acc", dev)
+    S, R = m.shape
+    D = acc.shape[2]
+    if l.shape != (S, R) or acc.shape[:2] != (S, R):
+        raise ValueError("shape mismatch between m/l/acc")
+    out = torch.empty((R, D), dtype=torch.float32, device=dev)
+    lse = torch.empty(R, dtype=torch.float32, device=dev) if want_lse else None
+    _native.call("attn_splitk_merge", _ptr(m), _ptr(l), _ptr(acc), S, R, D, _ptr(out), _ptr(lse),
+                 _stream(dev))
+    return out, lse
 
 
 def moe_swiglu_quant(gu: torch.Tensor, F: int | None = None):

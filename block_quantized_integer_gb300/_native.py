@@ -41,6 +41,7 @@ SIGNATURES = {
                                               P, SZ, P]),
     "import_gguf_q8_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
     "import_gguf_q4_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
+    "attn_splitk_merge": (ctypes.c_int, [P, P, P, I32, I64, I64, P, P, P]),
     "moe_swiglu_quant": (ctypes.c_int, [P, I64, I64, I64, P, P, P]),
     "moe_combine": (ctypes.c_int, [P, P, I64, I32, I64, P, P]),
 }

@@ -336,4 +336,14 @@ qg_status import_gguf_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t*
     return import_gguf(blocks, N, K, qw4, dw, true, stream);
 }
 
+qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, int32_t S,
+                            int64_t R, int64_t D, float* out, float* lse, cudaStream_t stream) {
+    if (S <= 0 || S > qg::splitk_merge_max_splits() || R < 0 || D <= 0) return QG_ERR_INVALID_ARG;
+    if (R == 0) return QG_OK;
+    if (!m || !l || !acc || !out) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)m | (uintptr_t)l | (uintptr_t)acc | (uintptr_t)out | (uintptr_t)lse) & 3u)
+        return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_splitk_merge(m, l, acc, S, R, D, out, lse, stream));
+}
+
 }  // extern "C"

@@ -69,6 +69,11 @@ cudaError_t launch_combine(const float* y, const float* w, int64_t T, int topk, 
 cudaError_t launch_gguf_import(const uint8_t* blocks, int64_t N, int64_t K, void* q, uint16_t* d,
                                bool q4, cudaStream_t s);
 
+// Split-K attention merge.
+int splitk_merge_max_splits();
+cudaError_t launch_splitk_merge(const float* m, const float* l, const float* acc, int S, int64_t R,
+                                int64_t D, float* out, float* lse, cudaStream_t s);
+
 // Test-only group-dot readout (qgemm_debug_group_dots).
 cudaError_t launch_fill_ones(float* v, int64_t n, cudaStream_t s);
 cudaError_t launch_one_hot_scales(uint16_t* dw, int64_t N, int64_t G, int64_t g, cudaStream_t s);

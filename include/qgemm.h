@@ -212,6 +212,21 @@ qg_status moe_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu,
 qg_status moe_combine(const float* y, const float* w, int64_t T, int32_t topk, int64_t N,
                       float* out, cudaStream_t stream);
 
+/* Split-K attention merge (the mining-card page, Implementation challenges 3:
+ * split-K FlashAttention partials merged with the log-sum-exp identity):
+ * for each row r (one head, one query) and split s with running max m_s,
+ * sum of exponentials l_s and unnormalised output acc_s,
+ *   m = max_s m_s,  l = sum_s exp(m_s - m) * l_s,  o = sum_s exp(m_s - m) * acc_s,
+ *   out[r] = o / l,  lse[r] = m + log(l),
+ * in binary32: the outputs summed over the splits in index order and l in a
+ * fixed order, so the result is deterministic.  Empty
+ * splits (m_s = -inf, l_s = 0) contribute nothing; a row with only empty
+ * splits gives out = 0 and lse = -inf.
+ *   m, l: float32 [S][R];  acc: float32 [S][R][D];  out: float32 [R][D];
+ *   lse: float32 [R] or NULL.  1 <= S <= 64. */
+qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, int32_t S,
+                            int64_t R, int64_t D, float* out, float* lse, cudaStream_t stream);
+
 /* grouped_qgemm_moe for callers that cannot allocate device memory: same
  * arguments, results and errors as grouped_qgemm_moe, minus the workspace.
  * (No counterpart in the pages this library follows: it exists for callers

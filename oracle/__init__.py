@@ -66,6 +66,7 @@ def _L():
             lib.orc_grouped_qgemm_moe.argtypes = [P, P, I64, P, I64, I32, I32, P, P, I32, I64, P, P]
             lib.orc_silu_mul.argtypes = [P, I64, I64, I64, P]
             lib.orc_import_gguf.argtypes = [P, I64, I64, ctypes.c_int, P, P]
+            lib.orc_splitk_merge.argtypes = [P, P, P, I32, I64, I64, P, P, P]
             lib.orc_moe_combine.argtypes = [P, P, I64, I32, I64, P, P]
             _lib = lib
     return _lib
@@ -229,4 +230,16 @@ def import_gguf(blocks: np.ndarray, N: int, K: int, wbits: int):
     d = np.empty((N, K // 32), np.uint16)
     _L().orc_import_gguf(_p(blocks), N, K, 1 if wbits == 4 else 0, _p(q), _p(d))
     return q, d
+
+
+def splitk_merge(m: np.ndarray, l: np.ndarray, acc: np.ndarray):
+    """(out [R, D], lse [R], mag [R, D]) in binary64 from split partials m, l [S, R], acc [S, R, D]."""
+    m, l, acc = _c(m, np.float32), _c(l, np.float32), _c(acc, np.float32)
+    S, R = m.shape
+    D = acc.shape[2]
+    out = np.empty((R, D), np.float64)
+    lse = np.empty(R, np.float64)
+    mag = np.empty((R, D), np.float64)
+    _L().orc_splitk_merge(_p(m), _p(l), _p(acc), S, R, D, _p(out), _p(lse), _p(mag))
+    return out, lse, mag
 

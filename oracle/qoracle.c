@@ -346,3 +346,33 @@ void orc_import_gguf(const uint8_t* blocks, int64_t N, int64_t K, int q4, uint8_
             memcpy(q + n * row_bytes + g * code_bytes, b + 2, (size_t)code_bytes);
         }
 }
+
+/* Split-K attention merge in binary64 (the mining-card page, Implementation
+ * challenges 3): m = max_s m_s, l = sum_s exp(m_s - m) l_s,
+ * o = sum_s exp(m_s - m) acc_s, out = o / l, lse = m + log(l).  Empty splits
+ * (m_s = -inf) contribute nothing; an all-empty row gives out = 0, lse = -inf.
+ * m, l [S][R], acc [S][R][D]; out [R][D], lse [R], mag [R][D] = sum_s
+ * exp(m_s - m) |acc_s| / l (the magnitude a binary32 sum is measured against). */
+void orc_splitk_merge(const float* m, const float* l, const float* acc, int32_t S, int64_t R,
+                      int64_t D, double* out, double* lse, double* mag) {
+    for (int64_t r = 0; r < R; ++r) {
+        double mg = -INFINITY;
+        for (int32_t s = 0; s < S; ++s)
+            if ((double)m[s * R + r] > mg) mg = (double)m[s * R + r];
+        double lg = 0.0;
+        for (int32_t s = 0; s < S; ++s)
+            if (m[s * R + r] != -INFINITY) lg += exp((double)m[s * R + r] - mg) * (double)l[s * R + r];
+        lse[r] = lg > 0.0 ? mg + log(lg) : -INFINITY;
+        for (int64_t c = 0; c < D; ++c) {
+            double o = 0.0, a = 0.0;
+            for (int32_t s = 0; s < S; ++s) {
+                if (m[s * R + r] == -INFINITY) continue;
+                double w = exp((double)m[s * R + r] - mg), v = (double)acc[(s * R + r) * D + c];
+                o += w * v;
+                a += w * fabs(v);
+            }
+            out[r * D + c] = lg > 0.0 ? o / lg : 0.0;
+            mag[r * D + c] = lg > 0.0 ? a / lg : 0.0;
+        }
+    }
+}

@@ -132,3 +132,13 @@ def test_gguf_import_validation(lib):
     assert f(NUL, 4, 64, B, C, S) == 1
     assert f(ctypes.c_void_p(0x10001), 4, 64, B, C, S) == 2     # blocks 2-byte aligned
     assert lib.import_gguf_q4_0(A, 4, 64, ctypes.c_void_p(0x20008), C, S) == 2
+
+
+def test_splitk_merge_validation(lib):
+    f = lib.attn_splitk_merge
+    assert f(A, B, C, 0, 4, 128, D, NUL, S) == 1          # S >= 1
+    assert f(A, B, C, 65, 4, 128, D, NUL, S) == 1         # S <= 64
+    assert f(A, B, C, 4, 4, 0, D, NUL, S) == 1            # D >= 1
+    assert f(A, B, C, 4, 0, 128, D, NUL, S) == 0          # R == 0: no-op
+    assert f(A, NUL, C, 4, 4, 128, D, NUL, S) == 1
+    assert f(A, B, C, 4, 4, 128, ctypes.c_void_p(0x40002), NUL, S) == 2

@@ -522,3 +522,32 @@ def test_gguf_import_bit_exact(wbits, N, K):
     q_ref, d_ref = oracle.import_gguf(blocks.reshape(-1), N, K, wbits)
     assert np.array_equal(to_np(qt).view(np.uint8), q_ref.view(np.uint8))
     assert np.array_equal(to_np(dt).view(np.uint16), d_ref)
+
+
+# ------------------------------------------------------------------ split-K attention merge
+
+@pytest.mark.parametrize("S,R,D", [(1, 5, 128), (4, 300, 128), (64, 37, 100), (7, 1024, 256)])
+def test_splitk_merge_vs_oracle(S, R, D):
+    rng = np.random.default_rng(500 + S + R + D)
+    m = (rng.standard_normal((S, R)) * 4.0).astype(np.float32)
+    l = (rng.random((S, R)) * 30.0 + 1.0).astype(np.float32)
+    acc = (rng.standard_normal((S, R, D)) * l[:, :, None]).astype(np.float32)
+    if S > 1:
+        m[1, :R // 2] = -np.inf                             # empty splits
+        l[1, :R // 2] = 0.0
+        acc[1, :R // 2] = 0.0
+        m[:, -1] = -np.inf                                  # a row with no key at all
+        l[:, -1] = 0.0
+        acc[:, -1] = 0.0
+    out, lse = qg.attn_splitk_merge(to_dev(m), to_dev(l), to_dev(acc))
+    _sync()
+    ref, ref_lse, mag = oracle.splitk_merge(m, l, acc)
+    o = to_np(out).astype(np.float64)
+    assert np.all(np.abs(o - ref) <= 2e-6 * mag + 1e-30)
+    ls = to_np(lse).astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.all(np.abs(ls[fin] - ref_lse[fin]) <= 1e-6 * np.maximum(1.0, np.abs(ref_lse[fin])))
+    assert np.all(ls[~fin] == -np.inf) and np.all(o[~fin] == 0.0)
+    out2, _ = qg.attn_splitk_merge(to_dev(m), to_dev(l), to_dev(acc))
+    _sync()
+    assert torch.equal(out, out2)

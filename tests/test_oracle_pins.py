@@ -504,3 +504,63 @@ def test_gguf_import_round_trip(wbits):
     assert blocks.size == N * (K // 32) * (34 if wbits == 8 else 18)
     q2, d2 = oracle.import_gguf(blocks, N, K, wbits)
     assert np.array_equal(q2.view(np.uint8), q.view(np.uint8)) and np.array_equal(d2, d)
+
+
+# ---------------------------------------------------------------- split-K attention merge
+
+def _partials(scores, values, bounds):
+    """Per-split partials from the definition of softmax attention (numpy, binary64)."""
+    S = len(bounds) - 1
+    R, T = scores.shape
+    D = values.shape[2]
+    m = np.full((S, R), -np.inf)
+    l = np.zeros((S, R))
+    acc = np.zeros((S, R, D))
+    for s in range(S):
+        a, b = bounds[s], bounds[s + 1]
+        if a == b:
+            continue
+        x = scores[:, a:b]
+        m[s] = x.max(axis=1)
+        e = np.exp(x - m[s][:, None])
+        l[s] = e.sum(axis=1)
+        acc[s] = np.einsum("rt,rtd->rd", e, values[:, a:b])
+    return m, l, acc
+
+
+def test_splitk_merge_equals_unsplit_softmax():
+    """Merging the splits of a row gives softmax(scores) @ values and log-sum-exp of the
+    scores, however the keys are split (including empty splits)."""
+    rng = np.random.default_rng(77)
+    R, T, D = 6, 50, 16
+    scores = rng.standard_normal((R, T)) * 3.0
+    values = rng.standard_normal((R, T, D))
+    p = np.exp(scores - scores.max(axis=1, keepdims=True))
+    ref = np.einsum("rt,rtd->rd", p / p.sum(axis=1, keepdims=True), values)
+    ref_lse = np.log(np.exp(scores).sum(axis=1))
+    for bounds in ([0, T], [0, 10, 10, 33, T], list(range(0, T + 1, 5))):
+        m, l, acc = _partials(scores, values, bounds)
+        out, lse, mag = oracle.splitk_merge(m.astype(np.float32), l.astype(np.float32),
+                                            acc.astype(np.float32))
+        assert np.allclose(out, ref, rtol=1e-5, atol=1e-6)     # binary32 partials in
+        assert np.allclose(lse, ref_lse, rtol=1e-6, atol=1e-6)
+        assert np.all(mag >= np.abs(out) - 1e-12)
+
+
+def test_splitk_merge_single_split_and_empty_rows():
+    rng = np.random.default_rng(78)
+    acc = rng.standard_normal((1, 3, 8)).astype(np.float32)
+    m = np.array([[0.5, -2.0, 3.0]], np.float32)
+    l = np.array([[2.0, 4.0, 0.5]], np.float32)
+    out, lse, _ = oracle.splitk_merge(m, l, acc)
+    assert np.allclose(out, acc[0] / l[0][:, None], rtol=1e-15)
+    assert np.allclose(lse, m[0] + np.log(l[0]), rtol=1e-15)
+    me = np.full((3, 2), -np.inf, np.float32)
+    me[1, 0] = 1.0
+    le = np.zeros((3, 2), np.float32)
+    le[1, 0] = 3.0
+    acce = np.zeros((3, 2, 4), np.float32)
+    acce[1, 0] = [3.0, 6.0, -3.0, 0.0]
+    out, lse, _ = oracle.splitk_merge(me, le, acce)
+    assert np.array_equal(out[0], [1.0, 2.0, -1.0, 0.0]) and np.isclose(lse[0], 1.0 + np.log(3.0))
+    assert np.array_equal(out[1], np.zeros(4)) and lse[1] == -np.inf
