@@ -422,6 +422,75 @@ def moe_layer_section(dev, peaks, reps=20):
     return res
 
 
+def next_rows_section(dev, peaks, reps=20):
+    """The HBM-bound kernels of the rows beyond the hot path, each on a
+    representative size, as algorithmic GB/s against the measured HBM peak
+    (L2 flushed before every timed call)."""
+    import torch
+    import block_quantized_integer_gb300 as qg
+    g = torch.Generator(device="cpu").manual_seed(20261202 + 7)
+    scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+
+    def timeit(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            scrub.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = {}
+    # activation quantization (hot-path row a1) at its largest workload: the
+    # long-context prefill activations, 18432 x 17408 binary32 (1.28 GB in)
+    Mq, Kq = 18432, 17408
+    xq = torch.randn((Mq, Kq), generator=g).to(dev)
+    qxq = torch.empty((Mq, Kq), dtype=torch.int8, device=dev)
+    dxq = torch.empty((Mq, Kq // 32), dtype=torch.float32, device=dev)
+    ms = timeit(lambda: qg.quantize_act_q8(xq, qxq, dxq))
+    nb = Mq * Kq * (4 + 1 + 4 / 32)
+    out["quantize_act_q8"] = {"shape": f"{Mq}x{Kq}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    del xq, qxq, dxq
+    # SwiGLU + re-quantization on the MoE workload's gate/up output (7576 x 2048 -> 7576 x 1024)
+    P, F = 7576, 1024
+    gu = torch.randn((P, 2 * F), generator=g).to(dev)
+    ms = timeit(lambda: qg.moe_swiglu_quant(gu, F))
+    nb = P * 2 * F * 4 + P * F * (1 + 4 / 32)
+    out["swiglu_quant"] = {"shape": f"{P}x{2 * F} -> {P}x{F}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    # router-weighted combine: 947 tokens x top-8 rows of 2048
+    T, topk, N = 947, 8, 2048
+    y = torch.randn((T * topk, N), generator=g).to(dev)
+    w = torch.rand((T, topk), generator=g).to(dev)
+    o = torch.empty((T, N), device=dev)
+    ms = timeit(lambda: qg.moe_combine(y, w, out=o))
+    nb = T * topk * N * 4 + T * topk * 4 + T * N * 4
+    out["moe_combine"] = {"shape": f"{T}x{topk}x{N}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    # GGUF Q8_0 import of a 12288 x 4096 matrix (34-byte blocks -> planes)
+    Nw, K = 12288, 4096
+    blocks = torch.randint(0, 256, (Nw * (K // 32) * 34,), dtype=torch.uint8, generator=g).to(dev)
+    ms = timeit(lambda: qg.import_gguf_q8_0(blocks, Nw, K))
+    nb = 2 * Nw * (K // 32) * 34
+    out["import_gguf_q8_0"] = {"shape": f"{Nw}x{K}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    # split-K attention merge: 16 splits x 32 heads x 2048 queries x D 128
+    S, R, D = 16, 32 * 2048, 128
+    mm = torch.randn((S, R), generator=g).to(dev)
+    ll = (torch.rand((S, R), generator=g) + 1.0).to(dev)
+    acc = torch.randn((S, R, D), generator=g).to(dev)
+    ms = timeit(lambda: qg.attn_splitk_merge(mm, ll, acc))
+    nb = S * R * (D + 2) * 4 + R * (D + 1) * 4
+    out["attn_splitk_merge"] = {"shape": f"S={S} R={R} D={D}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    for v in out.values():
+        v["frac_of_hbm"] = v["gbs"] / peaks["hbm_gbs"]
+    out["l2"] = "flushed before every timed call"
+    del scrub
+    return out
+
+
 # --------------------------------------------------------------------------- main
 
 def main():
@@ -431,7 +500,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
-    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "moe_layer", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "moe_layer", "next", "decode"],
+                    default=None,
                     help="run one section only (for profiling); prints its JSON")
     ap.add_argument("--reps", type=int, default=20, help="timed calls per prefill/MoE shape")
     args = ap.parse_args()
@@ -448,6 +518,8 @@ def main():
             out = moe_section(dev, peaks, reps=args.reps)
         elif args.only == "moe_layer":
             out = moe_layer_section(dev, peaks, reps=args.reps)
+        elif args.only == "next":
+            out = next_rows_section(dev, peaks, reps=args.reps)
         else:
             projs = make_decode(dev, 1)
             graphs = DecodeGraphs(projs)
@@ -562,6 +634,7 @@ def main():
         torch.cuda.empty_cache()
         line["moe"] = moe_section(dev, peaks, reps=args.reps)
         line["moe_layer"] = moe_layer_section(dev, peaks, reps=args.reps)
+        line["next_rows"] = next_rows_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
 
     if rank == 0:

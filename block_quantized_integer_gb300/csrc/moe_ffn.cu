@@ -32,48 +32,60 @@ __device__ __forceinline__ int quant127(float v, float d) {
 }
 
 // 8 threads per 32-group, 4 consecutive elements (one 16-byte load of gate
-// and one of up) per thread; a warp covers 4 groups.
+// and one of up) per thread; a warp covers 4 groups; U groups per thread have
+// their loads in flight together.
 __global__ void __launch_bounds__(256)
 swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t ldgu,
                     int8_t* __restrict__ qh, float* __restrict__ dh, bool vec_ok) {
+    constexpr int U = 2;
     const int64_t G = F / kGroup;
     const int64_t total = P * G;
     const int sub = threadIdx.x & 7;
     const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 3);
     const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
     const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
-    for (int64_t base = warp_first; base < total; base += stride) {   // whole warps iterate
-        const int64_t grp = base + ((threadIdx.x & 31) >> 3);
-        const bool active = grp < total;
-        const int64_t p = active ? grp / G : 0, g = active ? grp % G : 0;
-        float h[4] = {0.f, 0.f, 0.f, 0.f};
-        if (active) {
-            const float* gp = gu + p * ldgu + g * kGroup + sub * 4;
-            float4 a, b;
-            if (vec_ok) {
-                a = *reinterpret_cast<const float4*>(gp);
-                b = *reinterpret_cast<const float4*>(gp + F);
-            } else {
-                a = make_float4(gp[0], gp[1], gp[2], gp[3]);
-                b = make_float4(gp[F], gp[F + 1], gp[F + 2], gp[F + 3]);
+    for (int64_t base = warp_first; base < total; base += U * stride) {   // whole warps iterate
+        float4 a[U], b[U];
+        int64_t grp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            grp[u] = base + u * stride + ((threadIdx.x & 31) >> 3);
+            a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (grp[u] < total) {
+                const float* gp = gu + (grp[u] / G) * ldgu + (grp[u] % G) * kGroup + sub * 4;
+                if (vec_ok) {
+                    a[u] = *reinterpret_cast<const float4*>(gp);
+                    b[u] = *reinterpret_cast<const float4*>(gp + F);
+                } else {
+                    a[u] = make_float4(gp[0], gp[1], gp[2], gp[3]);
+                    b[u] = make_float4(gp[F], gp[F + 1], gp[F + 2], gp[F + 3]);
+                }
             }
-            h[0] = silu_mul(a.x, b.x);
-            h[1] = silu_mul(a.y, b.y);
-            h[2] = silu_mul(a.z, b.z);
-            h[3] = silu_mul(a.w, b.w);
         }
-        float m = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        const float d = __fdiv_rn(m, 127.0f);
-        if (active) {
-            const uint32_t packed = (uint32_t)(quant127(h[0], d) & 0xff) |
-                                    ((uint32_t)(quant127(h[1], d) & 0xff) << 8) |
-                                    ((uint32_t)(quant127(h[2], d) & 0xff) << 16) |
-                                    ((uint32_t)(quant127(h[3], d) & 0xff) << 24);
-            *reinterpret_cast<uint32_t*>(qh + p * F + g * kGroup + sub * 4) = packed;
-            if (sub == 0) dh[p * G + g] = d;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool active = grp[u] < total;
+            const int64_t p = active ? grp[u] / G : 0, g = active ? grp[u] % G : 0;
+            float h[4] = {0.f, 0.f, 0.f, 0.f};
+            if (active) {
+                h[0] = silu_mul(a[u].x, b[u].x);
+                h[1] = silu_mul(a[u].y, b[u].y);
+                h[2] = silu_mul(a[u].z, b[u].z);
+                h[3] = silu_mul(a[u].w, b[u].w);
+            }
+            float m = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            const float d = __fdiv_rn(m, 127.0f);
+            if (active) {
+                const uint32_t packed = (uint32_t)(quant127(h[0], d) & 0xff) |
+                                        ((uint32_t)(quant127(h[1], d) & 0xff) << 8) |
+                                        ((uint32_t)(quant127(h[2], d) & 0xff) << 16) |
+                                        ((uint32_t)(quant127(h[3], d) & 0xff) << 24);
+                *reinterpret_cast<uint32_t*>(qh + p * F + g * kGroup + sub * 4) = packed;
+                if (sub == 0) dh[p * G + g] = d;
+            }
         }
     }
 }

@@ -58,6 +58,7 @@ __device__ __forceinline__ uint16_t scale16(float amax, float qmax) {
 __global__ void __launch_bounds__(256)
 quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                        int8_t* __restrict__ qx, float* __restrict__ dx, bool vec_ok) {
+    constexpr int U = 2;                          // groups per thread in flight
     const int64_t G = K / kGroup;
     const int64_t total = M * G;
     const int sub = threadIdx.x & 7;
@@ -66,20 +67,29 @@ quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_
     // need the full warp), so the loop bound is rounded up to whole warps.
     const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
     const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
-    for (int64_t base = warp_first; base < total; base += stride) {
-        const int64_t grp = base + ((threadIdx.x & 31) >> 3);
-        const bool active = grp < total;
-        const int64_t m = active ? grp / G : 0, g = active ? grp % G : 0;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (active) v = load4(x + m * ldx + g * kGroup + sub * 4, vec_ok);
-        float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-        a = amax8(a);
-        const float d = __fdiv_rn(a, 127.0f);
-        if (active) {
-            uint32_t packed = pack_s8(quant1(v.x, d, -127, 127), quant1(v.y, d, -127, 127),
-                                      quant1(v.z, d, -127, 127), quant1(v.w, d, -127, 127));
-            *reinterpret_cast<uint32_t*>(qx + m * K + g * kGroup + sub * 4) = packed;
-            if (sub == 0) dx[m * G + g] = d;
+    for (int64_t base = warp_first; base < total; base += U * stride) {
+        float4 v[U];
+        int64_t grp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {             // all loads first
+            grp[u] = base + u * stride + ((threadIdx.x & 31) >> 3);
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (grp[u] < total)
+                v[u] = load4(x + (grp[u] / G) * ldx + (grp[u] % G) * kGroup + sub * 4, vec_ok);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool active = grp[u] < total;
+            const int64_t m = active ? grp[u] / G : 0, g = active ? grp[u] % G : 0;
+            float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+            a = amax8(a);
+            const float d = __fdiv_rn(a, 127.0f);
+            if (active) {
+                uint32_t packed = pack_s8(quant1(v[u].x, d, -127, 127), quant1(v[u].y, d, -127, 127),
+                                          quant1(v[u].z, d, -127, 127), quant1(v[u].w, d, -127, 127));
+                *reinterpret_cast<uint32_t*>(qx + m * K + g * kGroup + sub * 4) = packed;
+                if (sub == 0) dx[m * G + g] = d;
+            }
         }
     }
 }
