@@ -484,6 +484,16 @@ def next_rows_section(dev, peaks, reps=20):
     ms = timeit(lambda: qg.attn_splitk_merge(mm, ll, acc))
     nb = S * R * (D + 2) * 4 + R * (D + 1) * 4
     out["attn_splitk_merge"] = {"shape": f"S={S} R={R} D={D}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    # 3-bit KV codec: one head's keys over a 256 K context, D = 128
+    Tk, Dk = 262144, 128
+    xk = torch.randn((Tk, Dk), generator=g).to(dev)
+    ck, sk = qg.kv3_encode(xk)
+    ms = timeit(lambda: qg.kv3_encode(xk))
+    nb = Tk * Dk * 4 + Tk * (3 * Dk // 8 + 4)
+    out["kv3_encode"] = {"shape": f"T={Tk} D={Dk}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    ms = timeit(lambda: qg.kv3_decode(ck, sk, Dk))
+    out["kv3_decode"] = {"shape": f"T={Tk} D={Dk}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    del xk, ck, sk
     for v in out.values():
         v["frac_of_hbm"] = v["gbs"] / peaks["hbm_gbs"]
     out["l2"] = "flushed before every timed call"

@@ -27,7 +27,7 @@ __all__ = [
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
     "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
     "import_gguf_q8_0", "import_gguf_q4_0",
-    "attn_splitk_merge",
+    "attn_splitk_merge", "kv3_encode", "kv3_decode", "kv3_codebook",
     "moe_swiglu_quant", "moe_combine",
     "workspace_size", "debug_group_dots",
     "sm_count", "device_error",
@@ -169,6 +169,37 @@ def import_gguf_q8_0(blocks: torch.Tensor, N: int, K: int):
 def import_gguf_q4_0(blocks: torch.Tensor, N: int, K: int):
     """GGUF Q4_0 blocks (uint8, N * K/32 * 18 bytes) -> (qw4 uint8 [N, K/2], dw float16 [N, K/32])."""
     return _import_gguf("import_gguf_q4_0", blocks, N, K, 18, torch.uint8, K // 2)
+
+
+def kv3_encode(x: torch.Tensor):
+    """x float32 [T, D] (D = 64, 128, 256) -> (codes int32 [T, 3D/32] holding the bit-plane
+    words, scales float32 [T])."""
+    _need(x, torch.float32, "x", rows_strided=True)
+    T, D = x.shape
+    codes = torch.empty((T, 3 * D // 32), dtype=torch.int32, device=x.device)
+    scales = torch.empty(T, dtype=torch.float32, device=x.device)
+    _native.call("kv3_encode", _ptr(x), T, D, x.stride(0), _ptr(codes), _ptr(scales),
+                 _stream(x.device))
+    return codes, scales
+
+
+def kv3_decode(codes: torch.Tensor, scales: torch.Tensor, D: int):
+    """(codes int32 [T, 3D/32], scales float32 [T]) -> x^ float32 [T, D]."""
+    _need(codes, torch.int32, "codes")
+    _need(scales, torch.float32, "scales", codes.device)
+    T = codes.shape[0]
+    x = torch.empty((T, D), dtype=torch.float32, device=codes.device)
+    _native.call("kv3_decode", _ptr(codes), _ptr(scales), T, D, _ptr(x), D, _stream(codes.device))
+    return x
+
+
+def kv3_codebook():
+    """(levels [8], thresholds [7]) float32 numpy arrays of the codec in use."""
+    import numpy as np
+    lv = np.zeros(8, np.float32)
+    th = np.zeros(7, np.float32)
+    _native.load().qg_kv3_codebook(lv.ctypes.data_as(ctypes.c_void_p), th.ctypes.data_as(ctypes.c_void_p))
+    return lv, th
 
 
 def attn_splitk_merge(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, want_lse: bool = True):

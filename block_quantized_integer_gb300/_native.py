@@ -42,6 +42,9 @@ SIGNATURES = {
     "import_gguf_q8_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
     "import_gguf_q4_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
     "attn_splitk_merge": (ctypes.c_int, [P, P, P, I32, I64, I64, P, P, P]),
+    "kv3_encode": (ctypes.c_int, [P, I64, I32, I64, P, P, P]),
+    "kv3_decode": (ctypes.c_int, [P, P, I64, I32, P, I64, P]),
+    "qg_kv3_codebook": (None, [P, P]),
     "moe_swiglu_quant": (ctypes.c_int, [P, I64, I64, I64, P, P, P]),
     "moe_combine": (ctypes.c_int, [P, P, I64, I32, I64, P, P]),
 }

@@ -346,4 +346,26 @@ qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, in
     return from_cuda(qg::launch_splitk_merge(m, l, acc, S, R, D, out, lse, stream));
 }
 
+qg_status kv3_encode(const float* x, int64_t T, int32_t D, int64_t ldx, uint32_t* codes,
+                     float* scales, cudaStream_t stream) {
+    if (T < 0 || (D != 64 && D != 128 && D != 256) || ldx < D) return QG_ERR_INVALID_ARG;
+    if (T == 0) return QG_OK;
+    if (!x || !codes || !scales) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)x | (uintptr_t)codes | (uintptr_t)scales) & 3u) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_kv3_encode(x, T, D, ldx, codes, scales, stream));
+}
+
+qg_status kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int32_t D, float* x,
+                     int64_t ldx, cudaStream_t stream) {
+    if (T < 0 || (D != 64 && D != 128 && D != 256) || ldx < D) return QG_ERR_INVALID_ARG;
+    if (T == 0) return QG_OK;
+    if (!x || !codes || !scales) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)x | (uintptr_t)codes | (uintptr_t)scales) & 3u) return QG_ERR_ALIGNMENT;
+    return from_cuda(qg::launch_kv3_decode(codes, scales, T, D, x, ldx, stream));
+}
+
+void qg_kv3_codebook(float* levels, float* thresholds) {
+    if (levels && thresholds) qg::kv3_codebook(levels, thresholds);
+}
+
 }  // extern "C"

@@ -74,6 +74,13 @@ int splitk_merge_max_splits();
 cudaError_t launch_splitk_merge(const float* m, const float* l, const float* acc, int S, int64_t R,
                                 int64_t D, float* out, float* lse, cudaStream_t s);
 
+// 3-bit Walsh-Hadamard + Lloyd-Max KV codec.
+void kv3_codebook(float* levels, float* thresholds);
+cudaError_t launch_kv3_encode(const float* x, int64_t T, int D, int64_t ldx, uint32_t* codes,
+                              float* scales, cudaStream_t s);
+cudaError_t launch_kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int D,
+                              float* x, int64_t ldx, cudaStream_t s);
+
 // Test-only group-dot readout (qgemm_debug_group_dots).
 cudaError_t launch_fill_ones(float* v, int64_t n, cudaStream_t s);
 cudaError_t launch_one_hot_scales(uint16_t* dw, int64_t N, int64_t G, int64_t g, cudaStream_t s);

@@ -227,6 +227,26 @@ qg_status moe_combine(const float* y, const float* w, int64_t T, int32_t topk, i
 qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, int32_t S,
                             int64_t R, int64_t D, float* out, float* lse, cudaStream_t stream);
 
+/* 3-bit KV-cache codec (the mining-card page, Features: a 3-bit Walsh-Hadamard +
+ * Lloyd-Max KV cache; the pages name the steps only, the reading taken is):
+ *   y = H x / sqrt(D), H the Sylvester-ordered Hadamard matrix of order D;
+ *   s = sqrt(mean_j y_j^2) (binary32);
+ *   code_j = number of thresholds t_k <= y_j / s (0..7; all 0 when s = 0),
+ *            t_k = (l_k + l_{k+1}) / 2 over the 8 Lloyd-Max levels l_0 < .. < l_7
+ *            of the standard normal distribution (qg_kv3_codebook);
+ *   decode: x^ = H (s * l[code]) / sqrt(D).
+ * Codes of a vector: 3 bit planes, 3 D / 32 uint32 words; word b * (D/32) + e,
+ * bit L holds bit b of the code of element L * (D/32) + e.  D = 64, 128 or 256.
+ *   x: float32 [T][ldx] (ldx >= D);  codes: uint32 [T][3 D / 32];  scales: float32 [T].
+ * Encode decisions are taken in binary32 (butterflies, sqrt, IEEE division). */
+qg_status kv3_encode(const float* x, int64_t T, int32_t D, int64_t ldx, uint32_t* codes,
+                     float* scales, cudaStream_t stream);
+qg_status kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int32_t D, float* x,
+                     int64_t ldx, cudaStream_t stream);
+/* The 8 levels and 7 thresholds in use (HOST arrays), computed once by Lloyd's
+ * iteration in binary64 and rounded to binary32. */
+void qg_kv3_codebook(float* levels, float* thresholds);
+
 /* grouped_qgemm_moe for callers that cannot allocate device memory: same
  * arguments, results and errors as grouped_qgemm_moe, minus the workspace.
  * (No counterpart in the pages this library follows: it exists for callers

@@ -67,6 +67,10 @@ def _L():
             lib.orc_silu_mul.argtypes = [P, I64, I64, I64, P]
             lib.orc_import_gguf.argtypes = [P, I64, I64, ctypes.c_int, P, P]
             lib.orc_splitk_merge.argtypes = [P, P, P, I32, I64, I64, P, P, P]
+            lib.orc_kv3_codebook.argtypes = [P, P]
+            lib.orc_wht.argtypes = [P, I64, ctypes.c_int, P]
+            lib.orc_kv3_encode.argtypes = [P, I64, ctypes.c_int, P, P, P, P]
+            lib.orc_kv3_decode.argtypes = [P, P, I64, ctypes.c_int, P, P]
             lib.orc_moe_combine.argtypes = [P, P, I64, I32, I64, P, P]
             _lib = lib
     return _lib
@@ -242,4 +246,46 @@ def splitk_merge(m: np.ndarray, l: np.ndarray, acc: np.ndarray):
     mag = np.empty((R, D), np.float64)
     _L().orc_splitk_merge(_p(m), _p(l), _p(acc), S, R, D, _p(out), _p(lse), _p(mag))
     return out, lse, mag
+
+
+def kv3_codebook():
+    """(levels [8], thresholds [7]) of the 3-bit Lloyd-Max quantizer of N(0, 1), binary64."""
+    lv = np.empty(8, np.float64)
+    th = np.empty(7, np.float64)
+    _L().orc_kv3_codebook(_p(lv), _p(th))
+    return lv, th
+
+
+def wht(x: np.ndarray) -> np.ndarray:
+    """Orthonormal Walsh-Hadamard transform (Sylvester order) of each row, binary64."""
+    x = _c(x, np.float64)
+    T, D = x.shape
+    y = np.empty_like(x)
+    _L().orc_wht(_p(x), T, D, _p(y))
+    return y
+
+
+def kv3_encode(x: np.ndarray):
+    """x float32 [T, D] -> (codes uint32 [T, 3D/32], scales float32 [T], u binary64 [T, D])."""
+    x = _c(x, np.float32)
+    T, D = x.shape
+    _, th = kv3_codebook()
+    th32 = th.astype(np.float32)
+    codes = np.empty((T, 3 * D // 32), np.uint32)
+    scales = np.empty(T, np.float32)
+    u = np.empty((T, D), np.float64)
+    _L().orc_kv3_encode(_p(x), T, D, _p(th32), _p(codes), _p(scales), _p(u))
+    return codes, scales, u
+
+
+def kv3_decode(codes: np.ndarray, scales: np.ndarray, D: int) -> np.ndarray:
+    """(codes uint32 [T, 3D/32], scales float32 [T]) -> x^ binary64 [T, D]."""
+    codes = _c(codes, np.uint32)
+    scales = _c(scales, np.float32)
+    T = codes.shape[0]
+    lv, _ = kv3_codebook()
+    lv32 = lv.astype(np.float32)
+    out = np.empty((T, D), np.float64)
+    _L().orc_kv3_decode(_p(codes), _p(scales), T, D, _p(lv32), _p(out))
+    return out
 

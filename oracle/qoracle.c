@@ -376,3 +376,102 @@ void orc_splitk_merge(const float* m, const float* l, const float* acc, int32_t 
         }
     }
 }
+
+/* 3-bit KV-cache codec (the mining-card page, Features: 3-bit Walsh-Hadamard +
+ * Lloyd-Max KV cache; the steps are named only, so the reading is spelled out):
+ * codebook: the 8-level Lloyd-Max quantizer of the standard normal law, found
+ * by alternating the two optimality conditions (threshold = midpoint of its
+ * two levels; level = mean of the law over its cell) in binary64 from evenly
+ * spaced starting levels until they stop moving. */
+void orc_kv3_codebook(double* levels, double* thresholds) {
+    double lv[8], t[9];
+    for (int k = 0; k < 8; ++k) lv[k] = -2.0 + 4.0 * k / 7.0;
+    for (int it = 0; it < 20000; ++it) {
+        t[0] = -INFINITY;
+        t[8] = INFINITY;
+        for (int k = 1; k < 8; ++k) t[k] = (lv[k - 1] + lv[k]) / 2.0;
+        double moved = 0.0;
+        for (int k = 0; k < 8; ++k) {
+            /* mean of N(0,1) over (a, b): (phi(a) - phi(b)) / (Phi(b) - Phi(a)) */
+            double a = t[k], b = t[k + 1];
+            double pa = isinf(a) ? 0.0 : exp(-a * a / 2.0) / sqrt(2.0 * acos(-1.0));
+            double pb = isinf(b) ? 0.0 : exp(-b * b / 2.0) / sqrt(2.0 * acos(-1.0));
+            double Pa = isinf(a) ? 0.0 : 0.5 * erfc(-a / sqrt(2.0));
+            double Pb = isinf(b) ? 1.0 : 0.5 * erfc(-b / sqrt(2.0));
+            double c = (pa - pb) / (Pb - Pa);
+            moved = fmax(moved, fabs(c - lv[k]));
+            lv[k] = c;
+        }
+        if (moved == 0.0) break;
+    }
+    for (int k = 0; k < 8; ++k) levels[k] = lv[k];
+    for (int k = 0; k < 7; ++k) thresholds[k] = (lv[k] + lv[k + 1]) / 2.0;
+}
+
+/* Orthonormal Walsh-Hadamard transform of v[0..D) in place (Sylvester order),
+ * binary64: pairs (i, i + h) become (v_i + v_{i+h}, v_i - v_{i+h}) for
+ * h = 1, 2, .., D/2, then everything is divided by sqrt(D). */
+static void wht64(double* v, int D) {
+    for (int h = 1; h < D; h *= 2)
+        for (int i = 0; i < D; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                double a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+    double r = sqrt((double)D);
+    for (int j = 0; j < D; ++j) v[j] /= r;
+}
+
+void orc_wht(const double* x, int64_t T, int D, double* y) {
+    for (int64_t t = 0; t < T; ++t) {
+        memcpy(y + t * D, x + t * D, sizeof(double) * (size_t)D);
+        wht64(y + t * D, D);
+    }
+}
+
+/* Encode: y = H x / sqrt(D) and s = sqrt(mean y^2) in binary64; the stored
+ * scale is s rounded to binary32; code = number of binary32 thresholds <= y / s
+ * (0 when s == 0), with u = y / s kept for the caller.  Bit planes: word
+ * b * (D/32) + e, bit L = bit b of the code of element L * (D/32) + e. */
+void orc_kv3_encode(const float* x, int64_t T, int D, const float* thr32, uint32_t* codes,
+                    float* scales, double* u_out) {
+    int E = D / 32;
+    double y[256];
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < D; ++j) y[j] = (double)x[t * D + j];
+        wht64(y, D);
+        double ss = 0.0;
+        for (int j = 0; j < D; ++j) ss += y[j] * y[j];
+        double s = sqrt(ss / D);
+        scales[t] = (float)s;
+        uint32_t* w = codes + t * 3 * E;
+        for (int i = 0; i < 3 * E; ++i) w[i] = 0;
+        for (int j = 0; j < D; ++j) {
+            double u = s > 0.0 ? y[j] / s : 0.0;
+            int k = 0;
+            if (s > 0.0)
+                for (int i = 0; i < 7; ++i) k += u >= (double)thr32[i];
+            u_out[t * D + j] = u;
+            int L = j / E, e = j % E;
+            for (int b = 0; b < 3; ++b)
+                if ((k >> b) & 1) w[b * E + e] |= 1u << L;
+        }
+    }
+}
+
+/* Decode: y^_j = s * level[code_j] (binary32 levels), x^ = H y^ / sqrt(D), binary64. */
+void orc_kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int D,
+                    const float* lv32, double* out) {
+    int E = D / 32;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint32_t* w = codes + t * 3 * E;
+        double* y = out + t * D;
+        for (int j = 0; j < D; ++j) {
+            int L = j / E, e = j % E, k = 0;
+            for (int b = 0; b < 3; ++b) k |= (int)((w[b * E + e] >> L) & 1u) << b;
+            y[j] = (double)scales[t] * (double)lv32[k];
+        }
+        wht64(y, D);
+    }
+}

@@ -142,3 +142,23 @@ def test_splitk_merge_validation(lib):
     assert f(A, B, C, 4, 0, 128, D, NUL, S) == 0          # R == 0: no-op
     assert f(A, NUL, C, 4, 4, 128, D, NUL, S) == 1
     assert f(A, B, C, 4, 4, 128, ctypes.c_void_p(0x40002), NUL, S) == 2
+
+
+def test_kv3_library_codebook_matches_oracle(lib):
+    """The library computes its codebook on the host; it equals the oracle's, rounded."""
+    import numpy as np
+    import oracle
+    lv = np.zeros(8, np.float32)
+    th = np.zeros(7, np.float32)
+    lib.qg_kv3_codebook(lv.ctypes.data_as(ctypes.c_void_p), th.ctypes.data_as(ctypes.c_void_p))
+    olv, oth = oracle.kv3_codebook()
+    assert np.array_equal(lv, olv.astype(np.float32))
+    assert np.array_equal(th, oth.astype(np.float32))
+
+
+def test_kv3_validation(lib):
+    assert lib.kv3_encode(A, 4, 96, 96, B, C, S) == 1        # D not 64/128/256
+    assert lib.kv3_encode(A, 4, 128, 100, B, C, S) == 1      # ldx < D
+    assert lib.kv3_encode(A, 0, 128, 128, B, C, S) == 0      # T == 0: no-op
+    assert lib.kv3_encode(NUL, 4, 128, 128, B, C, S) == 1
+    assert lib.kv3_decode(A, ctypes.c_void_p(0x20002), 4, 128, C, 128, S) == 2

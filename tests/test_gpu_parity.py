@@ -551,3 +551,50 @@ def test_splitk_merge_vs_oracle(S, R, D):
     out2, _ = qg.attn_splitk_merge(to_dev(m), to_dev(l), to_dev(acc))
     _sync()
     assert torch.equal(out, out2)
+
+
+# ------------------------------------------------------------------ 3-bit WHT + Lloyd-Max KV codec
+
+def _kv3_codes(codes, D):
+    E = D // 32
+    c = codes.view(np.uint32).astype(np.int64)
+    k = np.zeros((c.shape[0], D), np.int64)
+    for j in range(D):
+        L, e = divmod(j, E)
+        for b in range(3):
+            k[:, j] |= ((c[:, b * E + e] >> L) & 1) << b
+    return k
+
+
+@pytest.mark.parametrize("T,D,pad", [(1000, 128, 0), (333, 64, 16), (257, 256, 0)])
+def test_kv3_encode_vs_oracle(T, D, pad):
+    """Scales within binary32 rounding of the binary64 oracle; codes identical except where
+    y / s lies within 1e-5 of a decision threshold."""
+    rng = np.random.default_rng(600 + T + D)
+    x = (rng.standard_normal((T, D + pad)) * rng.uniform(0.01, 10.0, (T, 1))).astype(np.float32)
+    x[0] = 0.0
+    xt = to_dev(x)[:, :D]
+    codes, scales = qg.kv3_encode(xt)
+    _sync()
+    oc, osc, u = oracle.kv3_encode(np.ascontiguousarray(x[:, :D]))
+    sc = to_np(scales).astype(np.float64)
+    assert np.all(np.abs(sc - osc) <= 4e-7 * osc)
+    kg, ko = _kv3_codes(to_np(codes), D), _kv3_codes(oc, D)
+    _, th = oracle.kv3_codebook()
+    near = np.min(np.abs(u[:, :, None] - th[None, None, :].astype(np.float32)), axis=2) < 1e-5
+    assert np.array_equal(kg[~near], ko[~near])
+    assert np.all(np.abs(kg[near] - ko[near]) <= 1)
+    assert np.all(kg[0] == 0) and sc[0] == 0.0
+
+
+@pytest.mark.parametrize("T,D", [(1000, 128), (77, 64), (300, 256)])
+def test_kv3_decode_vs_oracle(T, D):
+    """Decoding arbitrary codes and scales matches the binary64 oracle to binary32 rounding."""
+    rng = np.random.default_rng(700 + T + D)
+    codes = rng.integers(0, 2 ** 32, (T, 3 * D // 32), dtype=np.uint64).astype(np.uint32)
+    scales = (rng.random(T) * 5.0).astype(np.float32)
+    x = qg.kv3_decode(to_dev(codes.view(np.int32)), to_dev(scales), D)
+    _sync()
+    ref = oracle.kv3_decode(codes, scales, D)
+    bound = 1e-6 * scales[:, None].astype(np.float64) * 2.2 * np.sqrt(D) + 1e-30
+    assert np.all(np.abs(to_np(x).astype(np.float64) - ref) <= bound)

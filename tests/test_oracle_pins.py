@@ -564,3 +564,92 @@ def test_splitk_merge_single_split_and_empty_rows():
     out, lse, _ = oracle.splitk_merge(me, le, acce)
     assert np.array_equal(out[0], [1.0, 2.0, -1.0, 0.0]) and np.isclose(lse[0], 1.0 + np.log(3.0))
     assert np.array_equal(out[1], np.zeros(4)) and lse[1] == -np.inf
+
+
+# ---------------------------------------------------------------- 3-bit WHT + Lloyd-Max KV codec
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_wht_matches_sylvester_hadamard(D):
+    """The transform is scipy's Sylvester Hadamard matrix over sqrt(D), orthonormal and its
+    own inverse."""
+    sl = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(D)
+    x = rng.standard_normal((5, D))
+    H = sl.hadamard(D) / np.sqrt(D)
+    y = oracle.wht(x)
+    assert np.allclose(y, x @ H.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.wht(y), x, rtol=1e-12, atol=1e-12)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+
+def test_lloyd_max_codebook_conditions():
+    """Each level is the mean of N(0,1) over its cell and each threshold the midpoint of its
+    two levels (checked by numerical quadrature, not by the oracle's closed form); the
+    codebook is symmetric and its mean squared error is a local minimum."""
+    integ = pytest.importorskip("scipy.integrate")
+    lv, th = oracle.kv3_codebook()
+    assert np.all(np.diff(lv) > 0) and np.allclose(lv, -lv[::-1], atol=1e-15)
+    assert np.allclose(th, (lv[:-1] + lv[1:]) / 2, rtol=0, atol=1e-15)
+    phi = lambda t: np.exp(-t * t / 2) / np.sqrt(2 * np.pi)
+    edges = np.concatenate([[-np.inf], th, [np.inf]])
+    for k in range(8):
+        mass = integ.quad(phi, edges[k], edges[k + 1])[0]
+        mean = integ.quad(lambda t: t * phi(t), edges[k], edges[k + 1])[0] / mass
+        assert abs(mean - lv[k]) < 1e-9
+
+    def mse(levels):
+        e = np.concatenate([[-np.inf], (levels[:-1] + levels[1:]) / 2, [np.inf]])
+        return sum(integ.quad(lambda t: (t - levels[k]) ** 2 * phi(t), e[k], e[k + 1])[0]
+                   for k in range(8))
+
+    base = mse(lv)
+    assert 0.0344 < base < 0.0347                    # 3-bit Gaussian Lloyd-Max distortion
+    for k in (0, 3, 6):
+        for dlt in (1e-3, -1e-3):
+            p = lv.copy()
+            p[k] += dlt
+            assert mse(p) > base
+
+
+def _unpack_kv3(codes, D):
+    E = D // 32
+    T = codes.shape[0]
+    k = np.zeros((T, D), np.int64)
+    for j in range(D):
+        L, e = divmod(j, E)
+        for b in range(3):
+            k[:, j] |= ((codes[:, b * E + e].astype(np.int64) >> L) & 1) << b
+    return k
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_kv3_hadamard_column_closed_form(D):
+    """x = a Hadamard column: y = sqrt(D) e_k, s = 1, the code of y_k is 7 and every other
+    code is 4 (u = 0 sits on the middle threshold); decoding gives H (l_7 e_k + l_4 (1 - e_k))."""
+    sl = pytest.importorskip("scipy.linalg")
+    H = sl.hadamard(D).astype(np.float64)
+    k = 5
+    x = H[:, k].astype(np.float32)[None, :]
+    codes, scales, _ = oracle.kv3_encode(x)
+    assert scales[0] == 1.0
+    c = _unpack_kv3(codes, D)[0]
+    assert c[k] == 7 and np.all(np.delete(c, k) == 4)
+    lv, _ = oracle.kv3_codebook()
+    lv32 = lv.astype(np.float32).astype(np.float64)
+    yhat = np.full(D, lv32[4])
+    yhat[k] = lv32[7]
+    assert np.allclose(oracle.kv3_decode(codes, scales, D)[0], H @ yhat / np.sqrt(D), rtol=1e-12)
+
+
+def test_kv3_gaussian_distortion_and_zero_vector():
+    """On Gaussian vectors the relative error of decode(encode(x)) is the Lloyd-Max
+    distortion; a zero vector codes to scale 0 and decodes to 0."""
+    rng = np.random.default_rng(13)
+    D = 128
+    x = rng.standard_normal((4000, D)).astype(np.float32)
+    x[0] = 0.0
+    codes, scales, _ = oracle.kv3_encode(x)
+    xr = oracle.kv3_decode(codes, scales, D)
+    assert scales[0] == 0.0 and np.all(xr[0] == 0.0)
+    rel = np.sum((xr[1:] - x[1:]) ** 2) / np.sum(x[1:].astype(np.float64) ** 2)
+    assert 0.030 < rel < 0.040
