@@ -239,6 +239,23 @@ def decode_step(projs, timer=None):
             timer[1].record()
 
 
+def max_over_ranks(ms, dist=None, device="cuda"):
+    """The slowest rank's time: every rank contributes its own, all receive the max
+    (NCCL needs a device tensor, gloo a host one)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(world, bytes_per_step, steps, ms):
+    """Whole-job GB/s of `world` replicas, each moving bytes_per_step per step, timed by
+    the slowest rank over `steps` steps."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 def timed(fn, steps, warmup, dist=None, per_kernel=None):
     """Run fn warmup times, then time `steps` calls with CUDA events on the
     current stream, barrier + synchronize on both sides; max over ranks."""
@@ -259,11 +276,7 @@ def timed(fn, steps, warmup, dist=None, per_kernel=None):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist)
     kms = None
     if per_kernel:
         kms = statistics.mean(a.elapsed_time(b) for a, b in timers)
@@ -594,11 +607,11 @@ def main():
     time.sleep(0.3)
     ms, kms = timed(graphs.step, args.steps, args.warmup, dist, per_kernel=True)
     clocks = sampler.stop()
-    value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    value = replica_value(world, bytes_step, args.steps, ms)
 
     # end to end: pinned host x in, y out, every step
     ms_e2e, _ = timed(graphs.step_e2e, max(args.steps // 4, 10), 3, dist)
-    e2e = world * bytes_step * max(args.steps // 4, 10) / (ms_e2e * 1e-3) / 1e9
+    e2e = replica_value(world, bytes_step, max(args.steps // 4, 10), ms_e2e)
     h2d = sum(p["x_host"].numel() * 4 for p in projs)
     d2h = sum(p["y_host"].numel() * 4 for p in projs)
 
