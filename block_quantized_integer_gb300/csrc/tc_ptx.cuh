@@ -100,46 +100,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// 32 lanes x 32 bits, 16 consecutive columns: r[i] = column (taddr.col + i) of this lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr) : "memory");
-}
-
-// 32 lanes x 32 bits, 32 consecutive columns
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
-          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr) : "memory");
-}
-
-// 16 lanes x 256 bits, repeated over 4 blocks of 8 columns (32 columns): for
+// 16 lanes x 256 bits, repeated over 2 blocks of 8 columns (16 columns): for
 // block j, thread t holds lane (t / 4) columns 8j + 2 (t % 4) + {0, 1} in
 // r[4j], r[4j + 1] and lane (t / 4 + 8), same columns, in r[4j + 2], r[4j + 3].
-__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr) : "memory");
-}
-
-// As tmem_ld16x256b_x4 over 2 blocks of 8 columns (16 columns, 8 registers).
 __device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -163,16 +126,6 @@ __device__ __forceinline__ uint64_t pack2u(uint32_t a, uint32_t b) {
     return r;
 }
 
-// y2 (two binary32 in one 64-bit register) += {s0, s1} * ({w0, w1} * dx2)
-__device__ __forceinline__ void fma2_scaled(uint64_t& y2, uint32_t s0, uint32_t s1, float w0,
-                                            float w1, uint64_t dx2) {
-    asm("{\n\t.reg .b64 s, w, p;\n\t"
-        "mov.b64 s, {%1, %2};\n\t"
-        "mov.b64 w, {%3, %4};\n\t"
-        "mul.rn.f32x2 p, w, %5;\n\t"
-        "fma.rn.f32x2 %0, s, p, %0;\n\t}"
-        : "+l"(y2) : "r"(s0), "r"(s1), "f"(w0), "f"(w1), "l"(dx2));
-}
 __device__ __forceinline__ uint64_t pack2(float a, float b) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
