@@ -41,6 +41,7 @@ gemv_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
     const int64_t G = K / kGroup;
     const int64_t n0 = ((int64_t)blockIdx.x * SETS + warp / W) * R;
     const int split = warp % W;
+    pdl_wait();                               // x, scales and weights may come from the previous kernel
     float acc[R][M];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -194,13 +195,15 @@ cudaError_t launch_w(int W, const int8_t* qx, const float* dx, const uint8_t* qw
                      cudaStream_t s) {
     const int rows_per_block = (kWarps / W) * R;
     const int64_t blocks = (N + rows_per_block - 1) / rows_per_block;
+    // programmatic launch: the blocks may be scheduled while the previous
+    // kernel drains and wait for it in pdl_wait()
+    const dim3 g((unsigned)blocks), b(256);
     switch (W) {
-        case 1: gemv_kernel<M, R, kQ4, 1><<<blocks, 256, 0, s>>>(qx, dx, qw, dw, y, N, K, ldy); break;
-        case 2: gemv_kernel<M, R, kQ4, 2><<<blocks, 256, 0, s>>>(qx, dx, qw, dw, y, N, K, ldy); break;
-        case 4: gemv_kernel<M, R, kQ4, 4><<<blocks, 256, 0, s>>>(qx, dx, qw, dw, y, N, K, ldy); break;
-        default: gemv_kernel<M, R, kQ4, 8><<<blocks, 256, 0, s>>>(qx, dx, qw, dw, y, N, K, ldy); break;
+        case 1: return launch_pdl(gemv_kernel<M, R, kQ4, 1>, g, b, 0, s, qx, dx, qw, dw, y, N, K, ldy);
+        case 2: return launch_pdl(gemv_kernel<M, R, kQ4, 2>, g, b, 0, s, qx, dx, qw, dw, y, N, K, ldy);
+        case 4: return launch_pdl(gemv_kernel<M, R, kQ4, 4>, g, b, 0, s, qx, dx, qw, dw, y, N, K, ldy);
+        default: return launch_pdl(gemv_kernel<M, R, kQ4, 8>, g, b, 0, s, qx, dx, qw, dw, y, N, K, ldy);
     }
-    return cudaGetLastError();
 }
 
 // 4 rows per warp, one 512-byte step per row in flight per iteration: at

@@ -67,6 +67,8 @@ quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_
     // need the full warp), so the loop bound is rounded up to whole warps.
     const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
     const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
+    pdl_wait();                               // x may come from the previous kernel
+    pdl_release();                            // the next kernel may launch and wait for this one
     for (int64_t base = warp_first; base < total; base += U * stride) {
         float4 v[U];
         int64_t grp[U];
@@ -152,9 +154,8 @@ int grid_for(int64_t groups, int sm_count) {
 cudaError_t launch_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
                                    int8_t* qx, float* dx, cudaStream_t s) {
     const bool vec_ok = ((uintptr_t)x % 16 == 0) && (ldx % 4 == 0);
-    quantize_act_q8_kernel<<<grid_for(M * (K / kGroup), sm_count()), 256, 0, s>>>(
-        x, M, K, ldx, qx, dx, vec_ok);
-    return cudaGetLastError();
+    return launch_pdl(quantize_act_q8_kernel, dim3(grid_for(M * (K / kGroup), sm_count())), dim3(256),
+                      0, s, x, M, K, ldx, qx, dx, vec_ok);
 }
 
 cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* qw,
