@@ -435,6 +435,42 @@ def moe_layer_section(dev, peaks, reps=20):
     return res
 
 
+def decode_shapes_section(dev, peaks, reps=50):
+    """Each decode projection on its own (activation quantization + GEMV, the two
+    launches of one projection) at M = 1 and M = 4, L2 flushed before every timed
+    call (the 17.8 MB projection would otherwise be served from L2); median of reps."""
+    import torch
+    import block_quantized_integer_gb300 as qg
+    scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for M in (1, 4):
+        projs = make_decode(dev, M)
+        for p in projs:
+            def one():
+                qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
+                qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+            for _ in range(3):
+                one()
+            ts = []
+            for _ in range(reps):
+                scrub.fill_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                one()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            ms = statistics.median(ts)
+            nb = decode_bytes(M, [(p["N"], p["K"])])
+            out[f"M{M}_{p['N']}x{p['K']}"] = {"us": ms * 1e3, "gbs": nb / (ms * 1e-3) / 1e9,
+                                              "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del projs
+        torch.cuda.empty_cache()
+    out["l2"] = "flushed before every timed call"
+    del scrub
+    return out
+
+
 def next_rows_section(dev, peaks, reps=20):
     """The HBM-bound kernels of the rows beyond the hot path, each on a
     representative size, as algorithmic GB/s against the measured HBM peak
@@ -523,10 +559,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/MoE/M=4 sections")
-    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "moe_layer", "next", "decode"],
+    ap.add_argument("--only", choices=["prefill", "longctx", "moe", "moe_layer", "next", "decode",
+                                       "decode_shapes"],
                     default=None,
                     help="run one section only (for profiling); prints its JSON")
-    ap.add_argument("--reps", type=int, default=20, help="timed calls per prefill/MoE shape")
+    ap.add_argument("--reps", type=int, default=50, help="timed calls per prefill/MoE shape")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.only is not None:
@@ -543,6 +580,8 @@ def main():
             out = moe_layer_section(dev, peaks, reps=args.reps)
         elif args.only == "next":
             out = next_rows_section(dev, peaks, reps=args.reps)
+        elif args.only == "decode_shapes":
+            out = decode_shapes_section(dev, peaks, reps=args.reps)
         else:
             projs = make_decode(dev, 1)
             graphs = DecodeGraphs(projs)
@@ -649,6 +688,8 @@ def main():
         line["decode_m4"] = {"gbs": b4 * max(args.steps // 2, 10) / (ms4 * 1e-3) / 1e9,
                              "ms_per_step": ms4 / max(args.steps // 2, 10)}
         del g4, projs4
+        torch.cuda.empty_cache()
+        line["decode_shapes"] = decode_shapes_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
         line["prefill"] = prefill_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
