@@ -171,12 +171,13 @@ def test_qgemm_parity(algo, M, N, K, bits):
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("pad", [12, 13])            # even / odd ldy (vector / scalar stores)
 @pytest.mark.parametrize("algo", DENSE_ALGOS)
-def test_qgemm_ldy_and_determinism(algo):
+def test_qgemm_ldy_and_determinism(algo, pad):
     M, N, K = (4, 300, 640) if algo == qg.ALGO_GEMV else (40, 300, 768)
     qx, dx, qw, dw = _case(M, N, K, 8, 99)
     y_ref, mag = oracle.qgemm(qx, dx, qw, dw, 8)
-    big = torch.full((M, N + 12), 7.0, dtype=torch.float32, device=dev())
+    big = torch.full((M, N + pad), 7.0, dtype=torch.float32, device=dev())
     args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
     y1 = qg.qgemm_q8_0(*args, y=big[:, :N], algo=algo)
     _sync()
