@@ -149,6 +149,9 @@ gemv_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
             }
         }
     }
+    // every load of this block is done: the next kernel may start launching
+    // (it still waits for this grid to finish before it reads anything)
+    pdl_release();
     // warp reduction of the binary32 partials (fixed butterfly order)
 #pragma unroll
     for (int r = 0; r < R; ++r)
