@@ -47,6 +47,29 @@ __device__ __forceinline__ uint32_t nib_to_s8(uint32_t s) {
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
+// Division of 32-bit unsigned numerators by an invariant divisor d >= 1
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the unsigned case): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, t = mulhi(m, n) gives
+// n / d = (t + ((n - t) >> 1)) >> (l - 1) for every n < 2^32.  Replaces the
+// 64-bit software division of a flat index into (row, group) coordinates.
+struct FastDiv {
+    uint32_t d, m, l;
+    __host__ explicit FastDiv(uint32_t div = 1) : d(div), m(0), l(0) {
+        if (div > 1) {
+            uint32_t bits = 0;
+            while ((1ull << bits) < div) ++bits;          // ceil(log2 d)
+            l = bits;
+            m = (uint32_t)((((1ull << 32) * ((1ull << l) - div)) / div) + 1);
+        }
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        if (d == 1) return n;
+        const uint32_t t = __umulhi(m, n);
+        return (t + ((n - t) >> 1)) >> (l - 1);
+    }
+};
+
 // Programmatic dependent launch.  A kernel launched with launch_pdl() may start
 // while the previous kernel on the stream is still finishing; it must call
 // pdl_wait() before it reads anything that kernel may have written (the wait

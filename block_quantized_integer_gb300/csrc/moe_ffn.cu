@@ -34,9 +34,10 @@ __device__ __forceinline__ int quant127(float v, float d) {
 // 8 threads per 32-group, 4 consecutive elements (one 16-byte load of gate
 // and one of up) per thread; a warp covers 4 groups; U groups per thread have
 // their loads in flight together.
+template <bool kFast>
 __global__ void __launch_bounds__(256)
 swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t ldgu,
-                    int8_t* __restrict__ qh, float* __restrict__ dh, bool vec_ok) {
+                    int8_t* __restrict__ qh, float* __restrict__ dh, bool vec_ok, FastDiv fg) {
     constexpr int U = 2;
     const int64_t G = F / kGroup;
     const int64_t total = P * G;
@@ -52,7 +53,15 @@ swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t 
             grp[u] = base + u * stride + ((threadIdx.x & 31) >> 3);
             a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (grp[u] < total) {
-                const float* gp = gu + (grp[u] / G) * ldgu + (grp[u] % G) * kGroup + sub * 4;
+                int64_t pr, g;
+                if constexpr (kFast) {
+                    pr = fg.div((uint32_t)grp[u]);
+                    g = grp[u] - pr * G;
+                } else {
+                    pr = grp[u] / G;
+                    g = grp[u] % G;
+                }
+                const float* gp = gu + pr * ldgu + g * kGroup + sub * 4;
                 if (vec_ok) {
                     a[u] = *reinterpret_cast<const float4*>(gp);
                     b[u] = *reinterpret_cast<const float4*>(gp + F);
@@ -65,7 +74,6 @@ swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool active = grp[u] < total;
-            const int64_t p = active ? grp[u] / G : 0, g = active ? grp[u] % G : 0;
             float h[4] = {0.f, 0.f, 0.f, 0.f};
             if (active) {
                 h[0] = silu_mul(a[u].x, b[u].x);
@@ -83,8 +91,9 @@ swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t 
                                         ((uint32_t)(quant127(h[1], d) & 0xff) << 8) |
                                         ((uint32_t)(quant127(h[2], d) & 0xff) << 16) |
                                         ((uint32_t)(quant127(h[3], d) & 0xff) << 24);
-                *reinterpret_cast<uint32_t*>(qh + p * F + g * kGroup + sub * 4) = packed;
-                if (sub == 0) dh[p * G + g] = d;
+                // [P][F] codes and [P][G] scales at the flat group index
+                *reinterpret_cast<uint32_t*>(qh + grp[u] * kGroup + sub * 4) = packed;
+                if (sub == 0) dh[grp[u]] = d;
             }
         }
     }
@@ -132,8 +141,13 @@ int stream_grid(int64_t work) {
 cudaError_t launch_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t ldgu, int8_t* qh,
                                 float* dh, cudaStream_t s) {
     const bool vec_ok = ((uintptr_t)gu % 16 == 0) && (ldgu % 4 == 0) && (F % 4 == 0);
-    const int64_t threads = P * (F / kGroup) * 8;
-    swiglu_quant_kernel<<<stream_grid(threads), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok);
+    const int64_t total = P * (F / kGroup);
+    if (total < (1ll << 32))
+        swiglu_quant_kernel<true><<<stream_grid(total * 8), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok,
+                                                                       FastDiv((uint32_t)(F / kGroup)));
+    else
+        swiglu_quant_kernel<false><<<stream_grid(total * 8), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok,
+                                                                        FastDiv(1));
     return cudaGetLastError();
 }
 

@@ -55,9 +55,11 @@ __device__ __forceinline__ uint16_t scale16(float amax, float qmax) {
     return b;
 }
 
+// kFast: M * G < 2^32, flat group index split into (row, group) by FastDiv.
+template <bool kFast>
 __global__ void __launch_bounds__(256)
 quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
-                       int8_t* __restrict__ qx, float* __restrict__ dx, bool vec_ok) {
+                       int8_t* __restrict__ qx, float* __restrict__ dx, bool vec_ok, FastDiv fg) {
     constexpr int U = 2;                          // groups per thread in flight
     const int64_t G = K / kGroup;
     const int64_t total = M * G;
@@ -76,21 +78,29 @@ quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_
         for (int u = 0; u < U; ++u) {             // all loads first
             grp[u] = base + u * stride + ((threadIdx.x & 31) >> 3);
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (grp[u] < total)
-                v[u] = load4(x + (grp[u] / G) * ldx + (grp[u] % G) * kGroup + sub * 4, vec_ok);
+            if (grp[u] < total) {
+                int64_t m, g;
+                if constexpr (kFast) {
+                    m = fg.div((uint32_t)grp[u]);
+                    g = grp[u] - m * G;
+                } else {
+                    m = grp[u] / G;
+                    g = grp[u] % G;
+                }
+                v[u] = load4(x + m * ldx + g * kGroup + sub * 4, vec_ok);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool active = grp[u] < total;
-            const int64_t m = active ? grp[u] / G : 0, g = active ? grp[u] % G : 0;
-            float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-            a = amax8(a);
-            const float d = __fdiv_rn(a, 127.0f);
+            const float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+            const float d = __fdiv_rn(amax8(a), 127.0f);
             if (active) {
+                // codes and scales are stored at the flat group index: [M][G] row-major
                 uint32_t packed = pack_s8(quant1(v[u].x, d, -127, 127), quant1(v[u].y, d, -127, 127),
                                           quant1(v[u].z, d, -127, 127), quant1(v[u].w, d, -127, 127));
-                *reinterpret_cast<uint32_t*>(qx + m * K + g * kGroup + sub * 4) = packed;
-                if (sub == 0) dx[m * G + g] = d;
+                *reinterpret_cast<uint32_t*>(qx + grp[u] * kGroup + sub * 4) = packed;
+                if (sub == 0) dx[grp[u]] = d;
             }
         }
     }
@@ -154,8 +164,13 @@ int grid_for(int64_t groups, int sm_count) {
 cudaError_t launch_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t ldx,
                                    int8_t* qx, float* dx, cudaStream_t s) {
     const bool vec_ok = ((uintptr_t)x % 16 == 0) && (ldx % 4 == 0);
-    return launch_pdl(quantize_act_q8_kernel, dim3(grid_for(M * (K / kGroup), sm_count())), dim3(256),
-                      0, s, x, M, K, ldx, qx, dx, vec_ok);
+    const int64_t total = M * (K / kGroup);
+    const dim3 grid(grid_for(total, sm_count())), block(256);
+    if (total < (1ll << 32))
+        return launch_pdl(quantize_act_q8_kernel<true>, grid, block, 0, s, x, M, K, ldx, qx, dx, vec_ok,
+                          FastDiv((uint32_t)(K / kGroup)));
+    return launch_pdl(quantize_act_q8_kernel<false>, grid, block, 0, s, x, M, K, ldx, qx, dx, vec_ok,
+                      FastDiv(1));
 }
 
 cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* qw,
