@@ -238,7 +238,11 @@ qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, in
  * Codes of a vector: 3 bit planes, 3 D / 32 uint32 words; word b * (D/32) + e,
  * bit L holds bit b of the code of element L * (D/32) + e.  D = 64, 128 or 256.
  *   x: float32 [T][ldx] (ldx >= D);  codes: uint32 [T][3 D / 32];  scales: float32 [T].
- * Encode decisions are taken in binary32 (butterflies, sqrt, IEEE division). */
+ * Encode decisions are taken in binary32: z = H x unnormalised, then
+ * code bits from z_j >= sqrt(sum z^2) * (t_k / sqrt(D)) (the same test as
+ * y_j / s >= t_k for s > 0); s = sqrt(sum z^2) / D.  Codes can therefore differ
+ * from an exact evaluation only where y_j / s lies within binary32 rounding of
+ * a threshold. */
 qg_status kv3_encode(const float* x, int64_t T, int32_t D, int64_t ldx, uint32_t* codes,
                      float* scales, cudaStream_t stream);
 qg_status kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int32_t D, float* x,
