@@ -45,7 +45,7 @@ def decode_bytes(M, shapes):
 
 # DRAM bytes (read + write) of one lm-head GEMV launch, from the ncu capture
 # summarised in profiles/gemv_q8_lmhead_151936x4096_m1.md (same kernel build).
-LM_HEAD_TRAFFIC_BYTES = 661.260800e6 + 2.979840e6
+LM_HEAD_TRAFFIC_BYTES = 661.244928e6 + 3.205376e6
 
 
 def load_peaks():

@@ -183,14 +183,21 @@ def kv3_encode(x: torch.Tensor):
     return codes, scales
 
 
-def kv3_decode(codes: torch.Tensor, scales: torch.Tensor, D: int):
-    """(codes int32 [T, 3D/32], scales float32 [T]) -> x^ float32 [T, D]."""
+def kv3_decode(codes: torch.Tensor, scales: torch.Tensor, D: int, out: torch.Tensor = None):
+    """(codes int32 [T, 3D/32], scales float32 [T]) -> x^ float32 [T, D] (written into
+    `out`, rows may be strided, when given)."""
     _need(codes, torch.int32, "codes")
     _need(scales, torch.float32, "scales", codes.device)
     T = codes.shape[0]
-    x = torch.empty((T, D), dtype=torch.float32, device=codes.device)
-    _native.call("kv3_decode", _ptr(codes), _ptr(scales), T, D, _ptr(x), D, _stream(codes.device))
-    return x
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.float32, device=codes.device)
+    else:
+        _need(out, torch.float32, "out", codes.device, rows_strided=True)
+        if tuple(out.shape) != (T, D):
+            raise ValueError(f"out must be [{T}, {D}], got {tuple(out.shape)}")
+    _native.call("kv3_decode", _ptr(codes), _ptr(scales), T, D, _ptr(out), out.stride(0),
+                 _stream(codes.device))
+    return out
 
 
 def kv3_codebook():

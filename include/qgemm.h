@@ -231,7 +231,9 @@ qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, in
  * Lloyd-Max KV cache; the pages name the steps only, the reading taken is):
  *   y = H x / sqrt(D), H the Sylvester-ordered Hadamard matrix of order D;
  *   s = sqrt(mean_j y_j^2) (binary32);
- *   code_j = number of thresholds t_k <= y_j / s (0..7; all 0 when s = 0),
+ *   code_j = number of thresholds t_k <= y_j / s (0..7; all 0 when s = 0;
+ *            the codebook is symmetric about 0 and an exact tie on the
+ *            negative side goes to the level of larger magnitude),
  *            t_k = (l_k + l_{k+1}) / 2 over the 8 Lloyd-Max levels l_0 < .. < l_7
  *            of the standard normal distribution (qg_kv3_codebook);
  *   decode: x^ = H (s * l[code]) / sqrt(D).
@@ -239,8 +241,9 @@ qg_status attn_splitk_merge(const float* m, const float* l, const float* acc, in
  * bit L holds bit b of the code of element L * (D/32) + e.  D = 64, 128 or 256.
  *   x: float32 [T][ldx] (ldx >= D);  codes: uint32 [T][3 D / 32];  scales: float32 [T].
  * Encode decisions are taken in binary32: z = H x unnormalised, then
- * code bits from z_j >= sqrt(sum z^2) * (t_k / sqrt(D)) (the same test as
- * y_j / s >= t_k for s > 0); s = sqrt(sum z^2) / D.  Codes can therefore differ
+ * |z_j| against sqrt(sum z^2) * (t_k / sqrt(D)) for the positive thresholds
+ * and the sign of z_j (the same test as y_j / s against t_k for s > 0);
+ * s = sqrt(sum z^2) / D.  Codes can therefore differ
  * from an exact evaluation only where y_j / s lies within binary32 rounding of
  * a threshold. */
 qg_status kv3_encode(const float* x, int64_t T, int32_t D, int64_t ldx, uint32_t* codes,

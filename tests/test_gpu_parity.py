@@ -567,17 +567,20 @@ def _kv3_codes(codes, D):
     return k
 
 
-@pytest.mark.parametrize("T,D,pad", [(1000, 128, 0), (333, 64, 16), (257, 256, 0)])
-def test_kv3_encode_vs_oracle(T, D, pad):
+# (row stride, row offset): 16-byte rows take the vector path, the others the scalar one;
+# T not a multiple of the vectors a warp takes per step (32 / (D / 32))
+@pytest.mark.parametrize("T,D,pad,off", [(1000, 128, 0, 0), (333, 64, 16, 0), (257, 256, 0, 0),
+                                         (201, 128, 3, 0), (129, 64, 5, 1), (77, 256, 4, 2)])
+def test_kv3_encode_vs_oracle(T, D, pad, off):
     """Scales within binary32 rounding of the binary64 oracle; codes identical except where
     y / s lies within 1e-5 of a decision threshold."""
     rng = np.random.default_rng(600 + T + D)
     x = (rng.standard_normal((T, D + pad)) * rng.uniform(0.01, 10.0, (T, 1))).astype(np.float32)
     x[0] = 0.0
-    xt = to_dev(x)[:, :D]
+    xt = to_dev(x)[:, off:off + D]
     codes, scales = qg.kv3_encode(xt)
     _sync()
-    oc, osc, u = oracle.kv3_encode(np.ascontiguousarray(x[:, :D]))
+    oc, osc, u = oracle.kv3_encode(np.ascontiguousarray(x[:, off:off + D]))
     sc = to_np(scales).astype(np.float64)
     assert np.all(np.abs(sc - osc) <= 4e-7 * osc)
     kg, ko = _kv3_codes(to_np(codes), D), _kv3_codes(oc, D)
@@ -599,3 +602,28 @@ def test_kv3_decode_vs_oracle(T, D):
     ref = oracle.kv3_decode(codes, scales, D)
     bound = 1e-6 * scales[:, None].astype(np.float64) * 2.2 * np.sqrt(D) + 1e-30
     assert np.all(np.abs(to_np(x).astype(np.float64) - ref) <= bound)
+
+
+@pytest.mark.parametrize("T,D,pad,off", [(97, 128, 3, 1), (65, 64, 2, 0), (33, 256, 5, 3)])
+def test_kv3_decode_unaligned(T, D, pad, off):
+    """Code words one word off 16-byte alignment and strided, unaligned output rows (the
+    scalar paths) decode like the aligned call; round trip of an encode stays close."""
+    rng = np.random.default_rng(800 + T + D)
+    W = 3 * D // 32
+    codes = rng.integers(0, 2 ** 32, (T, W), dtype=np.uint64).astype(np.uint32)
+    scales = (rng.random(T) * 5.0).astype(np.float32)
+    flat = torch.zeros(T * W + 1, dtype=torch.int32, device="cuda")
+    cview = flat[1:].view(T, W)
+    cview.copy_(to_dev(codes.view(np.int32)))
+    big = torch.full((T, D + pad), -7.0, device="cuda")
+    out = big[:, off:off + D]
+    qg.kv3_decode(cview, to_dev(scales), D, out=out)
+    aligned = qg.kv3_decode(to_dev(codes.view(np.int32)), to_dev(scales), D)
+    _sync()
+    assert torch.equal(out, aligned)
+    keep = torch.ones(D + pad, dtype=torch.bool)
+    keep[off:off + D] = False
+    assert torch.all(big[:, keep.cuda()] == -7.0)
+    ref = oracle.kv3_decode(codes, scales, D)
+    bound = 1e-6 * scales[:, None].astype(np.float64) * 2.2 * np.sqrt(D) + 1e-30
+    assert np.all(np.abs(to_np(out).astype(np.float64) - ref) <= bound)
