@@ -52,6 +52,7 @@ constexpr int GA = 2;                  // groups per A stage = one pair (64 bina
 constexpr int NO = 4;                  // operand slots: binary16 A stage + binary16 B pair
 constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q8 / 8 Q4 groups)
 constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
+constexpr int NPMAX = 8;               // MoE pair slots at most (narrow tiles: 8 x 2 x 32 columns)
 constexpr int SCG = 8;                 // groups per scale stage
 constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
@@ -75,7 +76,7 @@ constexpr int OFF_B = OFF_A + NO * A_STAGE;
 constexpr int OFF_F16 = OFF_B + NB * B_STAGE;
 constexpr int OFF_SC = OFF_F16 + NO * F16_PAIR;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_STAGE;
-constexpr int NUM_BARS = 3 * NO + 2 * NB + NP + 2 * NSC + 1;
+constexpr int NUM_BARS = 3 * NO + 2 * NB + 2 * NPMAX + 2 * NSC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -90,9 +91,10 @@ constexpr uint32_t kSleepHintNs = 20000;             // a waiter sleeps until th
 // full_a: TMA A stage landed; full_ops: the converters saw full_a and wrote
 // the binary16 B pair, so both operands of the slot are ready; done: the
 // MMAs of the pair completed (one commit: operand slot free and the pair's
-// accumulators readable); tempty: the epilogue has read the TMEM pair slot.
+// accumulators readable); tempty: the epilogue has read the TMEM pair slot;
+// afull (MoE tiles): the MMAs into a TMEM pair slot completed.
 struct Bars {
-    uint32_t full_a, full_ops, done, full_b, empty_b, tempty, full_sc, empty_sc, drain;
+    uint32_t full_a, full_ops, done, full_b, empty_b, tempty, afull, full_sc, empty_sc, drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
@@ -103,7 +105,8 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
     b.full_b = b.done + 8 * NO;
     b.empty_b = b.full_b + 8 * NB;
     b.tempty = b.empty_b + 8 * NB;
-    b.full_sc = b.tempty + 8 * NP;
+    b.afull = b.tempty + 8 * NPMAX;
+    b.full_sc = b.afull + 8 * NPMAX;
     b.empty_sc = b.full_sc + 8 * NSC;
     b.drain = b.empty_sc + 8 * NSC;
     return b;
@@ -251,6 +254,141 @@ __device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, int G, const Group
     return T;
 }
 
+// Columns a MoE tile's pair slot gives each of its two groups: the tile's
+// rows rounded up to 32, 64 or 128 (the MMA N is the rows rounded up to 16).
+__device__ __forceinline__ int slot_width(int rows) { return rows <= 32 ? 32 : (rows <= 64 ? 64 : BN); }
+
+// One MoE output tile of the epilogue (the dense epilogue is inline in the
+// kernel).  TMEM lanes = weight rows (dw per lane, binary16 as stored),
+// columns = the segment's rows (dx per column).  Fragments and arithmetic are
+// the dense epilogue's (16-lane x 256-bit reads, y += (S * dw) * dx on packed
+// f32x2), but warp w covers its TMEM quarter (w % 4) over CW columns from
+// (w / 4) CW, with CW = 8, 16 or 32 taken from the tile's row count (at most
+// 32, 64 or 128 columns in use): short segments keep all 16 warps busy on a
+// quarter of the reads each instead of leaving 12 idle.  Each output is still
+// one thread's running sum over the groups in order.  The pair slots follow
+// the MMA issuer's ring: slot r mod (8 / 4 / 2) of 2 x 4 CW columns, waited on
+// through its afull barrier (apar: per slot, the parity of its next phase).
+// Returns false when a wait gave up.
+template <int CW>
+__device__ __forceinline__ bool epilogue_tile(const Bars& B, const uint8_t* smem, uint32_t tmem_base,
+                                              volatile int* abort, int PAIRS, uint32_t& r, uint32_t& apar,
+                                              uint32_t& sc,
+                                              int warp, int lane, int t, int trows, int64_t M, int G,
+                                              int n_tiles, float* __restrict__ y, int64_t N, int64_t ldy,
+                                              const GroupedArgs& ga) {
+    constexpr int NJ = CW / 8;                          // 8-column blocks per warp
+    constexpr int W = 4 * CW;                           // columns of one group in a slot
+    constexpr uint32_t kSlotMask = (uint32_t)(2 * BN / W) - 1;
+    const int q = warp & 3;                             // TMEM lane quarter
+    const int cb = (warp >> 2) * CW;
+    const int c2 = 2 * (lane & 3);
+    const int rb = q * 32 + (lane >> 2);                // lanes rb + 8 i, i = 0..3
+    // a warp with no valid output (short MoE segments, ragged last tile)
+    // keeps the barrier protocol but skips the readout and math
+    const bool live = cb < trows;
+    uint64_t acc[4][NJ];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) acc[i][j] = 0ull;
+    for (int pl = 0; pl < PAIRS; ++pl, ++r) {
+        const int g0 = 2 * pl, ps = (int)(r & kSlotMask);
+        const int slot = (int)(sc % NSC);
+        if (g0 % SCG == 0 && !wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort)) return false;
+        // every warp, live or not, waits for the slot's MMAs before releasing it
+        if (!wait_bar<true>(B.afull + 8 * ps, (apar >> ps) & 1u, abort)) return false;
+        apar ^= 1u << ps;
+        tc_fence_after();
+        if (live) {
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ps * 2 * W + cb);
+            const float* scf = reinterpret_cast<const float*>(smem + OFF_SC + slot * SC_STAGE);
+            // per-lane scales of the pair's two groups
+            float2 lsc[4];
+            const __half2* dws = reinterpret_cast<const __half2*>(smem + OFF_SC + slot * SC_STAGE + SC_DX);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lsc[i] = __half22float2(dws[((rb + 8 * i) * SCG + (g0 % SCG)) / 2]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // per-column scale pairs of group g0 + h for the warp's column blocks
+                uint64_t csc[NJ];
+                const float* dxc = scf + (cb + c2) * SCG + (g0 % SCG) + h;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) csc[j] = pack2(dxc[8 * j * SCG], dxc[(8 * j + 1) * SCG]);
+                if constexpr (CW == 8) {
+                    const uint32_t ta = taddr + h * W;
+                    uint32_t s0[4], s1[4];
+                    tmem_ld16x256b_x1(ta, s0);                 // lanes rb, rb + 8
+                    tmem_ld16x256b_x1(ta + (16u << 16), s1);   // lanes rb + 16, rb + 24
+                    tmem_wait_ld();
+                    if (h == 1) {                              // pair slot read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float d = h ? lsc[i].y : lsc[i].x;
+                        const uint32_t* sv = i < 2 ? s0 : s1;
+                        const int e = 2 * (i & 1);
+                        fma_f32x2(acc[i][0], mul_f32x2(pack2u(sv[e], sv[e + 1]), pack2(d, d)), csc[0]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < CW / 16; ++k) {        // 16-column halves
+                        const uint32_t ta = taddr + h * W + 16 * k;
+                        uint32_t s0[8], s1[8];
+                        tmem_ld16x256b_x2(ta, s0);             // lanes rb, rb + 8
+                        tmem_ld16x256b_x2(ta + (16u << 16), s1);   // lanes rb + 16, rb + 24
+                        tmem_wait_ld();
+                        if (h == 1 && k == CW / 16 - 1) {      // pair slot read out
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float d = h ? lsc[i].y : lsc[i].x;
+                            const uint64_t d2 = pack2(d, d);
+                            const uint32_t* sv = i < 2 ? s0 : s1;
+                            const int e = 2 * (i & 1);
+                            fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), d2), csc[2 * k]);
+                            fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), d2), csc[2 * k + 1]);
+                        }
+                    }
+                }
+            }
+        } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+        }
+        if ((g0 + 1) % SCG == SCG - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
+            ++sc;
+        }
+    }
+    if (!live) return true;
+    const Tile T = tile_at<true>(t, M, G, ga, n_tiles);        // fetched again: fewer live registers
+    // lane rb + 8 i = output column n0 + rb + 8 i; column = segment row
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = cb + 8 * j + c2 + e;
+            if (r < T.rows) {
+                float* yr = y + (int64_t)ga.perm[T.m0 + r] * ldy + T.n0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 v = unpack2(acc[i][j]);
+                    if (T.n0 + rb + 8 * i < N) yr[rb + 8 * i] = e ? v.y : v.x;
+                }
+            }
+        }
+    return true;
+}
+
 // Persistent: CTA b takes tiles b, b + gridDim.x, ...  All roles walk the same
 // tile sequence; ring positions and barrier phases run on across tiles.
 template <bool kQ4, bool kGrouped>
@@ -282,7 +420,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             mbar_init(B.full_b + 8 * i, 1);
             mbar_init(B.empty_b + 8 * i, CONV_WARPS);
         }
-        for (int i = 0; i < NP; ++i) mbar_init(B.tempty + 8 * i, EPI_WARPS);
+        for (int i = 0; i < NPMAX; ++i) {
+            mbar_init(B.tempty + 8 * i, EPI_WARPS);
+            mbar_init(B.afull + 8 * i, 1);
+        }
         for (int i = 0; i < NSC; ++i) {
             mbar_init(B.full_sc + 8 * i, 1);
             mbar_init(B.empty_sc + 8 * i, EPI_WARPS);
@@ -361,42 +502,88 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (lane == 0) {
             bool issued_any = false, ok = true;
             uint32_t p = 0;                                 // pair counter (A stage = pair)
-            // MoE tiles put the 128 weight rows on the MMA's M side (TMEM lanes)
-            // and the segment's rows on N, rounded up to 16: short segments
-            // cost short MMAs.  The next tile's row count is fetched a tile early.
-            int next_rows = (kGrouped && t0 < num_tiles) ? tile_at<kGrouped>(t0, M, G, ga, n_tiles).rows : BM;
-            for (int t = t0; t < num_tiles && ok; t += dt) {
-                uint32_t idesc = IDESC;
-                if constexpr (kGrouped) {
-                    const int nt = min(BM, max(16, (next_rows + 15) & ~15));
-                    idesc = idesc_f16_f32(BN, nt);
+            if constexpr (kGrouped) {
+                // MoE tiles put the 128 weight rows on the MMA's M side (TMEM
+                // lanes) and the segment's rows on N, rounded up to 16: short
+                // segments cost short MMAs.  A tile of at most W = 32 / 64 / 128
+                // columns packs 8 / 4 / 2 pair slots (2 x W columns each) into
+                // the 512 TMEM columns, so the MMAs run up to that many pairs
+                // ahead of the epilogue.  The epilogue waits on the slot's own
+                // afull barrier (never more than one phase ahead: a slot is
+                // reused only after tempty); when W changes, every slot of the
+                // old layout is read out before the new layout is written.
+                uint32_t tpar = 0;                          // per slot: parity of its uses so far
+                uint32_t r = 0;                             // ring position in the current layout
+                int width = 0;
+                int next_rows = t0 < num_tiles ? tile_at<kGrouped>(t0, M, G, ga, n_tiles).rows : BM;
+                for (int t = t0; t < num_tiles && ok; t += dt) {
+                    const int rows = next_rows;
                     if (t + dt < num_tiles) next_rows = tile_at<kGrouped>(t + dt, M, G, ga, n_tiles).rows;
-                }
-                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                    const int so = (int)(p % NO), ps = (int)(p % NP);
-                    const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
-                    // both probes go out back to back; one branch on the pair
-                    const bool ready = mbar_try_wait(B.full_ops + 8 * so, po) &
-                                       mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
-                    if (!ready) {
-                        if (!(ok = wait_bar<false>(B.full_ops + 8 * so, po, abort))) break;
-                        if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
+                    const int nt = min(BM, max(16, (rows + 15) & ~15));
+                    const uint32_t idesc = idesc_f16_f32(BN, nt);
+                    const int W = slot_width(rows);
+                    if (W != width) {
+                        for (int b = 0; b < NPMAX && ok; ++b)
+                            ok = wait_bar<false>(B.tempty + 8 * b, ((tpar >> b) & 1u) ^ 1u, abort);
+                        if (!ok) break;
+                        width = W;
+                        r = 0;
                     }
-                    tc_fence_after();
-                    const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
-                    const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
-                    const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const uint64_t da = smem_desc_sw128(a_s + h * 64 + j * 32);
-                            const uint64_t db = smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512);
-                            if constexpr (kGrouped) mma_f16(d + h * BN, db, da, idesc, j);
-                            else mma_f16(d + h * BN, da, db, idesc, j);
+                    const uint32_t nps_mask = (uint32_t)(2 * BN / W) - 1;   // 8, 4 or 2 slots
+                    for (int pl = 0; pl < PAIRS; ++pl, ++p, ++r) {
+                        const int so = (int)(p % NO), b = (int)(r & nps_mask);
+                        const uint32_t po = (uint32_t)((p / NO) & 1), tp = ((tpar >> b) & 1u) ^ 1u;
+                        const bool ready = mbar_try_wait(B.full_ops + 8 * so, po) &
+                                           mbar_try_wait(B.tempty + 8 * b, tp);
+                        if (!ready) {
+                            if (!(ok = wait_bar<false>(B.full_ops + 8 * so, po, abort))) break;
+                            if (!(ok = wait_bar<false>(B.tempty + 8 * b, tp, abort))) break;
                         }
-                    mma_commit(B.done + 8 * so);
-                    issued_any = true;
+                        tc_fence_after();
+                        const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
+                        const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
+                        const uint32_t d = tmem_base + (uint32_t)(b * 2 * W);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint64_t da = smem_desc_sw128(a_s + h * 64 + j * 32);
+                                const uint64_t db = smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512);
+                                mma_f16(d + h * W, db, da, idesc, j);
+                            }
+                        mma_commit(B.done + 8 * so);
+                        mma_commit(B.afull + 8 * b);
+                        tpar ^= 1u << b;
+                        issued_any = true;
+                    }
+                }
+            } else {
+                for (int t = t0; t < num_tiles && ok; t += dt) {
+                    for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                        const int so = (int)(p % NO), ps = (int)(p % NP);
+                        const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
+                        // both probes go out back to back; one branch on the pair
+                        const bool ready = mbar_try_wait(B.full_ops + 8 * so, po) &
+                                           mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
+                        if (!ready) {
+                            if (!(ok = wait_bar<false>(B.full_ops + 8 * so, po, abort))) break;
+                            if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_s = sbase + OFF_A + so * A_STAGE;
+                        const uint32_t b_s = sbase + OFF_F16 + so * F16_PAIR;
+                        const uint32_t d = tmem_base + (uint32_t)(ps * 2 * BN);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint64_t da = smem_desc_sw128(a_s + h * 64 + j * 32);
+                                const uint64_t db = smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512);
+                                mma_f16(d + h * BN, da, db, IDESC, j);
+                            }
+                        mma_commit(B.done + 8 * so);
+                        issued_any = true;
+                    }
                 }
             }
             if (*abort && issued_any) {
@@ -432,150 +619,137 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // TMEM is read in 16-lane x 256-bit fragments: per 8-column block a
-        // thread holds 2 adjacent columns of 2 lanes (8 apart), so each scale
-        // pair serves 2 partials, and the column pairs go through packed
-        // f32x2 multiplies and FMAs.  Warp w covers the 32 lanes of its TMEM
-        // quarter (w % 4) and 32 columns.
-        //   dense: lanes = A rows (dx per lane), columns = B rows (dw per
-        //     column; the dw stage holds each 32-column block permuted so that
-        //     a thread's 8 columns are contiguous: 2 x 16-byte loads a group);
-        //   MoE: lanes = weight rows (dw per lane, binary16 as stored),
-        //     columns = the segment's rows (dx per column).
-        // Both compute y += (S * dw) * dx with the same roundings.
-        const int q = warp & 3;                             // TMEM lane quarter
-        const int cb = (warp >> 2) * 32;                    // 32 columns per warp
-        const int c2 = 2 * (lane & 3);
-        const int rb = q * 32 + (lane >> 2);                // lanes rb + 8 i, i = 0..3
-        uint32_t p = 0, sc = 0;
-        bool ok = true;
-        for (int t = t0; t < num_tiles && ok; t += dt) {
-            // a warp with no valid output (short MoE segments, ragged last
-            // tile) keeps the barrier protocol but skips the readout and math
-            const int trows = (int)tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
-            const bool live = kGrouped ? cb < trows : q * 32 < trows;
-            uint64_t acc[4][4];
+        if constexpr (kGrouped) {
+            // MoE tiles: columns per warp from the segment's row count
+            uint32_t r = 0, apar = 0, sc = 0;
+            int width = 0;
+            for (int t = t0; t < num_tiles; t += dt) {
+                const int trows = (int)tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+                const int W = slot_width(trows);
+                if (W != width) {                           // the issuer restarts its ring too
+                    width = W;
+                    r = 0;
+                }
+                bool ok;
+                if (W == 32)
+                    ok = epilogue_tile<8>(B, smem, tmem_base, abort, PAIRS, r, apar, sc, warp, lane, t, trows, M, G, n_tiles, y, N, ldy, ga);
+                else if (W == 64)
+                    ok = epilogue_tile<16>(B, smem, tmem_base, abort, PAIRS, r, apar, sc, warp, lane, t, trows, M, G, n_tiles, y, N, ldy, ga);
+                else
+                    ok = epilogue_tile<32>(B, smem, tmem_base, abort, PAIRS, r, apar, sc, warp, lane, t, trows, M, G, n_tiles, y, N, ldy, ga);
+                if (!ok) break;
+            }
+        } else {
+            // Dense tiles.  TMEM is read in 16-lane x 256-bit fragments: per
+            // 8-column block a thread holds 2 adjacent columns of 2 lanes (8
+            // apart), so each scale pair serves 2 partials, and the column pairs
+            // go through packed f32x2 multiplies and FMAs.  Warp w covers the 32
+            // lanes of its TMEM quarter (w % 4) and 32 columns.  Lanes = A rows
+            // (dx per lane), columns = B rows (dw per column; the dw stage holds
+            // each 32-column block permuted so that a thread's 8 columns are
+            // contiguous: 2 x 16-byte loads a group).  y += (S * dw) * dx, the
+            // roundings of the MoE epilogue.
+            const int q = warp & 3;                             // TMEM lane quarter
+            const int cb = (warp >> 2) * 32;                    // 32 columns per warp
+            const int c2 = 2 * (lane & 3);
+            const int rb = q * 32 + (lane >> 2);                // lanes rb + 8 i, i = 0..3
+            uint32_t p = 0, sc = 0;
+            bool ok = true;
+            for (int t = t0; t < num_tiles && ok; t += dt) {
+                // a warp with no valid output (ragged last tile) keeps the
+                // barrier protocol but skips the readout and math
+                const int trows = (int)tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+                const bool live = q * 32 < trows;
+                uint64_t acc[4][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
-            for (int pl = 0; pl < PAIRS; ++pl, ++p) {
-                const int g0 = 2 * pl, ps = (int)(p % NP), so = (int)(p % NO);
-                const int slot = (int)(sc % NSC);
-                if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
-                if (!(ok = wait_bar<true>(B.done + 8 * so, (uint32_t)((p / NO) & 1), abort))) break;
-                tc_fence_after();
-                if (live) {
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)(ps * 2 * BN + cb);
-                    const float* scf = reinterpret_cast<const float*>(smem + OFF_SC + slot * SC_STAGE);
-                    // per-lane scales of the pair's two groups
-                    float2 lsc[4];
-                    if constexpr (kGrouped) {
-                        const __half2* dws = reinterpret_cast<const __half2*>(smem + OFF_SC + slot * SC_STAGE + SC_DX);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) lsc[i] = __half22float2(dws[((rb + 8 * i) * SCG + (g0 % SCG)) / 2]);
-                    } else {
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
+                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                    const int g0 = 2 * pl, ps = (int)(p % NP), so = (int)(p % NO);
+                    const int slot = (int)(sc % NSC);
+                    if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
+                    if (!(ok = wait_bar<true>(B.done + 8 * so, (uint32_t)((p / NO) & 1), abort))) break;
+                    tc_fence_after();
+                    if (live) {
+                        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                               (uint32_t)(ps * 2 * BN + cb);
+                        const float* scf = reinterpret_cast<const float*>(smem + OFF_SC + slot * SC_STAGE);
+                        // per-lane scales of the pair's two groups
+                        float2 lsc[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             lsc[i] = *reinterpret_cast<const float2*>(scf + (rb + 8 * i) * SCG + (g0 % SCG));
-                    }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        // per-column scale pairs of group g0 + h for column blocks 0..3
-                        uint64_t csc[4];
-                        if constexpr (kGrouped) {
-                            const float* dxc = scf + (cb + c2) * SCG + (g0 % SCG) + h;
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) csc[j] = pack2(dxc[8 * j * SCG], dxc[(8 * j + 1) * SCG]);
-                        } else {
+                        for (int h = 0; h < 2; ++h) {
+                            // per-column scale pairs of group g0 + h for column blocks 0..3
+                            uint64_t csc[4];
                             const float* dwp = scf + SC_DX / 4 + ((g0 % SCG) + h) * BN + cb + 4 * c2;
                             const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(dwp);
                             const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(dwp + 4);
                             csc[0] = wa.x; csc[1] = wa.y; csc[2] = wb.x; csc[3] = wb.y;
-                        }
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) {                  // 16-column halves
-                            const uint32_t ta = taddr + h * BN + 16 * k;
-                            uint32_t s0[8], s1[8];
-                            tmem_ld16x256b_x2(ta, s0);                 // lanes rb, rb + 8
-                            tmem_ld16x256b_x2(ta + (16u << 16), s1);   // lanes rb + 16, rb + 24
-                            tmem_wait_ld();
-                            if (h == 1 && k == 1) {                    // pair slot read out
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
-                            }
+                            for (int k = 0; k < 2; ++k) {                  // 16-column halves
+                                const uint32_t ta = taddr + h * BN + 16 * k;
+                                uint32_t s0[8], s1[8];
+                                tmem_ld16x256b_x2(ta, s0);                 // lanes rb, rb + 8
+                                tmem_ld16x256b_x2(ta + (16u << 16), s1);   // lanes rb + 16, rb + 24
+                                tmem_wait_ld();
+                                if (h == 1 && k == 1) {                    // pair slot read out
+                                    tc_fence_before();
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                                }
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float d = h ? lsc[i].y : lsc[i].x;
-                                const uint64_t d2 = pack2(d, d);
-                                const uint32_t* sv = i < 2 ? s0 : s1;
-                                const int e = 2 * (i & 1);
-                                if constexpr (kGrouped) {
-                                    fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), d2), csc[2 * k]);
-                                    fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), d2), csc[2 * k + 1]);
-                                } else {
+                                for (int i = 0; i < 4; ++i) {
+                                    const float d = h ? lsc[i].y : lsc[i].x;
+                                    const uint64_t d2 = pack2(d, d);
+                                    const uint32_t* sv = i < 2 ? s0 : s1;
+                                    const int e = 2 * (i & 1);
                                     fma_f32x2(acc[i][2 * k], mul_f32x2(pack2u(sv[e], sv[e + 1]), csc[2 * k]), d2);
                                     fma_f32x2(acc[i][2 * k + 1], mul_f32x2(pack2u(sv[4 + e], sv[4 + e + 1]), csc[2 * k + 1]), d2);
                                 }
                             }
                         }
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
                     }
-                } else {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B.tempty + 8 * ps);
+                    if ((g0 + 1) % SCG == SCG - 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
+                        ++sc;
+                    }
                 }
-                if ((g0 + 1) % SCG == SCG - 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(B.empty_sc + 8 * slot);
-                    ++sc;
-                }
-            }
-            if (!ok) break;
-            if (live) {
-                const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
-                if constexpr (kGrouped) {
-                    // lane rb + 8 i = output column n0 + rb + 8 i; column = segment row
+                if (!ok) break;
+                if (live) {
+                    const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
+                    {
+                        const int64_t col0 = T.n0 + cb + c2;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = rb + 8 * i;                   // tile row
+                            if (row < T.rows) {
+                                float* yr = y + (T.m0 + row) * ldy + col0;
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int r = cb + 8 * j + c2 + e;
-                            if (r < T.rows) {
-                                float* yr = y + (int64_t)ga.perm[T.m0 + r] * ldy + T.n0;
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
+                                for (int j = 0; j < 4; ++j) {
                                     const float2 v = unpack2(acc[i][j]);
-                                    if (T.n0 + rb + 8 * i < N) yr[rb + 8 * i] = e ? v.y : v.x;
-                                }
-                            }
-                        }
-                } else {
-                    const int64_t col0 = T.n0 + cb + c2;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int row = rb + 8 * i;                   // tile row
-                        if (row < T.rows) {
-                            float* yr = y + (T.m0 + row) * ldy + col0;
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float2 v = unpack2(acc[i][j]);
-                                const int64_t col = col0 + 8 * j;
-                                if (vec2 && col + 1 < N) {
-                                    *reinterpret_cast<float2*>(yr + 8 * j) = v;
-                                } else {
-                                    if (col < N) yr[8 * j] = v.x;
-                                    if (col + 1 < N) yr[8 * j + 1] = v.y;
+                                    const int64_t col = col0 + 8 * j;
+                                    if (vec2 && col + 1 < N) {
+                                        *reinterpret_cast<float2*>(yr + 8 * j) = v;
+                                    } else {
+                                        if (col < N) yr[8 * j] = v.x;
+                                        if (col + 1 < N) yr[8 * j + 1] = v.y;
+                                    }
                                 }
                             }
                         }
                     }
                 }
             }
+          }
         }
-    }
 
     tc_fence_before();
     __syncthreads();
@@ -636,16 +810,100 @@ transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t
     }
 }
 
-// MoE tile table: m-tile t of expert e (tile_offsets[e] <= t < tile_offsets[e+1])
-// covers sorted rows offsets[e] + (t - tile_offsets[e]) * BM onward.
-__global__ void __launch_bounds__(128)
-tile_info_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_offsets,
-                 int32_t E, int4* __restrict__ info) {
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
-        const int32_t end = offsets[e + 1];
-        int32_t m0 = offsets[e];
-        for (int32_t t = tile_offsets[e]; t < tile_offsets[e + 1]; ++t, m0 += BM)
-            info[t] = make_int4(m0, min(BM, end - m0), e, 0);
+// MoE tile table, ordered by slot width: first every tile of more than 64
+// rows (full 128-row tiles and long tails), then the tails of 33-64 rows, then
+// those of at most 32, each class in expert order.  A CTA walks the table with
+// a stride of the grid size, so its tiles change TMEM slot layout at most
+// twice per call (each change drains the pair-slot ring).  Each entry:
+// {first sorted row, rows, expert, 0}; the entry count equals tile_offsets[E].
+// One block of 1024 threads, experts taken 1024 at a time.
+__device__ __forceinline__ int width_class(int32_t rows) { return rows > 64 ? 0 : (rows > 32 ? 1 : 2); }
+
+__global__ void __launch_bounds__(1024)
+tile_info_kernel(const int32_t* __restrict__ offsets, int32_t E, int4* __restrict__ info) {
+    __shared__ int32_t part[3][32];
+    __shared__ int32_t run[3];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // tiles of expert e per class: full tiles and a tail of > 64 rows in
+    // class 0, a shorter tail in class 1 or 2
+    auto counts = [&](int e, int32_t (&c)[3]) {
+        c[0] = c[1] = c[2] = 0;
+        if (e >= E) return;
+        const int32_t n = offsets[e + 1] - offsets[e], tail = n % BM;
+        c[0] = n / BM;
+        if (tail > 0) ++c[width_class(tail)];
+    };
+    // exclusive block scan of c (per class); returns the chunk totals in tot
+    auto block_scan = [&](int32_t (&c)[3], int32_t (&ex)[3], int32_t (&tot)[3]) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            int32_t v = c[k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane == 31) part[k][wid] = v;
+            ex[k] = v - c[k];
+        }
+        __syncthreads();
+        if (wid == 0) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                int32_t v = part[k][lane];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                part[k][lane] = v;                      // inclusive over warps
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            ex[k] += wid > 0 ? part[k][wid - 1] : 0;
+            tot[k] = part[k][31];
+        }
+        __syncthreads();                                // part reused by the next chunk
+    };
+    // pass 1: class sizes
+    int32_t size[3] = {0, 0, 0};
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        int32_t c[3], ex[3], tot[3];
+        counts(e0 + tid, c);
+        block_scan(c, ex, tot);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) size[k] += tot[k];
+    }
+    if (tid == 0) {
+        run[0] = 0;
+        run[1] = size[0];
+        run[2] = size[0] + size[1];
+    }
+    __syncthreads();
+    // pass 2: placement
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        const int e = e0 + tid;
+        int32_t c[3], ex[3], tot[3];
+        counts(e, c);
+        block_scan(c, ex, tot);
+        if (e < E) {
+            const int32_t first = offsets[e], end = offsets[e + 1];
+            int32_t m0 = first;
+            int32_t at = run[0] + ex[0];
+            for (; end - m0 > 64; m0 += BM) info[at++] = make_int4(m0, min(BM, end - m0), e, 0);
+            if (end > m0) {
+                const int k = width_class(end - m0);
+                info[run[k] + ex[k]] = make_int4(m0, end - m0, e, 0);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) run[k] += tot[k];
+        }
+        __syncthreads();
     }
 }
 
@@ -796,7 +1054,7 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     // gather + widen the routed rows (count read on the device: offsets[E])
     widen_rows_kernel<<<widen_grid(P * (K / 16)), 256, 0, s>>>(qx, dx, P, K, a16, dxg, perm,
                                                                offsets + E, topk, x_row_mode);
-    tile_info_kernel<<<(E + 127) / 128, 128, 0, s>>>(offsets, tile_offsets, E, info);
+    tile_info_kernel<<<1, 1024, 0, s>>>(offsets, E, info);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;

@@ -111,6 +111,15 @@ __device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, uint32_t (&r)[
         : "r"(taddr) : "memory");
 }
 
+// One block of 8 columns of the same 16-lane x 256-bit shape: thread t holds
+// lane (t / 4) columns 2 (t % 4) + {0, 1} in r[0], r[1] and lane (t / 4 + 8)
+// in r[2], r[3].
+__device__ __forceinline__ void tmem_ld16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr) : "memory");
+}
+
 // packed binary32 pairs: d = a * b and acc = a * b + acc, element-wise, round to nearest
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     uint64_t d;
