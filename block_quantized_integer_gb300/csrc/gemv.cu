@@ -29,8 +29,12 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// Q8 at 2 <= M <= 4 with a K-split (W > 1) or M = 2: three resident blocks
+// per SM (<= 80 registers a thread, no spills) keep 24 warps' weight loads in
+// flight, which the stream needs to cover HBM latency; M = 1 fits three blocks
+// unforced.
 template <int M, int R, bool kQ4, int W>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, (!kQ4 && M >= 2 && M <= 4 && (W > 1 || M == 2)) ? 3 : 2)
 gemv_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
             const uint8_t* __restrict__ qw, const uint16_t* __restrict__ dw,
             float* __restrict__ y, int64_t N, int64_t K, int64_t ldy) {
@@ -218,10 +222,12 @@ constexpr int rows_per_warp(int M) { (void)M; return 4; }
 
 // K-split factor: enough blocks to fill the GPU a few times over, while each
 // warp keeps at least one full 512-byte step of weights per row.
-int gemv_split(int64_t N, int64_t K, bool q4, int sm, int R) {
+int gemv_split(int64_t M, int64_t N, int64_t K, bool q4, int sm, int R) {
     const int64_t row_bytes = q4 ? K / 2 : K;
     const int64_t want_blocks = (int64_t)sm * 8;
-    int W = 1;
+    // at M >= 2 the split starts at 2: the W = 1 kernel needs more registers
+    // than three resident blocks allow
+    int W = (M >= 2 && !q4 && row_bytes / 4 >= 512) ? 2 : 1;
     while (W < 8 && (N * W) / (kWarps * R) < want_blocks && row_bytes / (2 * W) >= 512) W *= 2;
     return W;
 }
@@ -234,7 +240,7 @@ cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N,
 #define QG_GEMV_CASE(MM)                                                                        \
     case MM: {                                                                                  \
         constexpr int R = rows_per_warp(MM);                                                    \
-        const int W = gemv_split(N, K, q4, sm, R);                                              \
+        const int W = gemv_split(MM, N, K, q4, sm, R);                                          \
         return q4 ? launch_w<MM, R, true>(W, qx, dx, w, dw, y, N, K, ldy, s)                    \
                   : launch_w<MM, R, false>(W, qx, dx, w, dw, y, N, K, ldy, s);                  \
     }

@@ -25,7 +25,7 @@ cudaError_t launch_quantize_act_q8(const float* x, int64_t M, int64_t K, int64_t
 cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* qw,
                                    uint16_t* dw, bool q4, cudaStream_t s);
 
-int gemv_split(int64_t N, int64_t K, bool q4, int sm, int R);
+int gemv_split(int64_t M, int64_t N, int64_t K, bool q4, int sm, int R);
 cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                         const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                         cudaStream_t s);
