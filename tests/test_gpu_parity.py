@@ -503,9 +503,11 @@ def test_moe_layer_end_to_end():
 
 # ------------------------------------------------------------------ GGUF block import
 
+# block counts 111, 38400 and 38528 (a multiple of 256 and not); off = 2: the input
+# 2 bytes past 16-byte alignment (the format only guarantees 2-byte alignment)
 @pytest.mark.parametrize("wbits", [8, 4])
-@pytest.mark.parametrize("N,K", [(37, 96), (300, 4096)])
-def test_gguf_import_bit_exact(wbits, N, K):
+@pytest.mark.parametrize("N,K,off", [(37, 96, 0), (300, 4096, 0), (301, 4096, 0), (301, 4096, 2)])
+def test_gguf_import_bit_exact(wbits, N, K, off):
     """The CUDA import equals the oracle byte for byte, and the imported weights give
     the same product as the same weights quantized planar."""
     rng = np.random.default_rng(90 + N + wbits)
@@ -518,7 +520,10 @@ def test_gguf_import_bit_exact(wbits, N, K):
     blocks[:, :, 1] = (d >> 8).astype(np.uint8)
     blocks[:, :, 2:] = q.view(np.uint8).reshape(N, G, cb)
     imp = qg.import_gguf_q8_0 if wbits == 8 else qg.import_gguf_q4_0
-    qt, dt = imp(to_dev(blocks.reshape(-1)), N, K)
+    flat = blocks.reshape(-1)
+    buf = torch.zeros(flat.size + off, dtype=torch.uint8, device="cuda")
+    buf[off:].copy_(to_dev(flat))
+    qt, dt = imp(buf[off:], N, K)
     _sync()
     q_ref, d_ref = oracle.import_gguf(blocks.reshape(-1), N, K, wbits)
     assert np.array_equal(to_np(qt).view(np.uint8), q_ref.view(np.uint8))
