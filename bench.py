@@ -152,22 +152,35 @@ def oracle_decode(shapes, M, budget_s, steps_hint):
 # --------------------------------------------------------------------------- GPU arm
 
 def make_decode(dev, M, seed_sub=0):
+    """The four decode projections.  Their activations live in one device buffer
+    (and one pinned host buffer), their outputs likewise, each projection's x and
+    y being views: the end-to-end step moves the inputs in and the outputs out
+    with one copy each (the keys x_all, x_all_host, y_all, y_all_host)."""
     import torch
     import block_quantized_integer_gb300 as qg
     from block_quantized_integer_gb300 import inputs
-    projs = []
-    for i, (N, K) in enumerate(inputs.DECODE_SHAPES):
+    shapes = inputs.DECODE_SHAPES
+    nx, ny = sum(M * K for _, K in shapes), sum(M * N for N, _ in shapes)
+    x_all = torch.empty(nx, dtype=torch.float32, device=dev)
+    y_all = torch.empty(ny, dtype=torch.float32, device=dev)
+    x_all_host = torch.empty(nx, dtype=torch.float32).pin_memory()
+    y_all_host = torch.empty(ny, dtype=torch.float32).pin_memory()
+    projs, ox, oy = [], 0, 0
+    for i, (N, K) in enumerate(shapes):
         w, x = inputs.decode_case(N, K, M=M, sub=i + seed_sub)
         wt = torch.from_numpy(w).to(dev)
         qw, dw = qg.quantize_weight_q8_0(wt)
         del wt
-        xt = torch.from_numpy(x).to(dev)
+        xt = x_all[ox:ox + M * K].view(M, K)
+        xt.copy_(torch.from_numpy(x))
+        x_all_host[ox:ox + M * K].copy_(torch.from_numpy(x).reshape(-1))
         qx = torch.empty((M, K), dtype=torch.int8, device=dev)
         dx = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
-        y = torch.empty((M, N), dtype=torch.float32, device=dev)
-        projs.append(dict(N=N, K=K, x=xt, qx=qx, dx=dx, qw=qw, dw=dw, y=y,
-                          x_host=torch.from_numpy(x).pin_memory(),
-                          y_host=torch.empty((M, N), dtype=torch.float32).pin_memory()))
+        y = y_all[oy:oy + M * N].view(M, N)
+        projs.append(dict(N=N, K=K, x=xt, qx=qx, dx=dx, qw=qw, dw=dw, y=y, x_all=x_all,
+                          y_all=y_all, x_all_host=x_all_host, y_all_host=y_all_host))
+        ox += M * K
+        oy += M * N
     torch.cuda.synchronize()
     return projs
 
@@ -181,7 +194,8 @@ class DecodeGraphs:
     graphs `head` (quantizations + the three small GEMVs) and `lm` (the
     lm-head GEMV alone) replay the same launches split in two, so that CUDA
     events can time the lm-head GEMV by itself;
-    graph `e2e` = host copies in, the whole step, host copies out."""
+    graph `e2e` = the inputs in from pinned host memory (one copy), the whole
+    step, the outputs out to pinned host memory (one copy)."""
 
     def __init__(self, projs):
         import torch
@@ -205,13 +219,12 @@ class DecodeGraphs:
             self._head(qg)
         with torch.cuda.graph(self.g_lm):
             self._lm(qg)
+        pk = projs[0]
         with torch.cuda.graph(self.g_e2e):
-            for p in projs:
-                p["x"].copy_(p["x_host"], non_blocking=True)
+            pk["x_all"].copy_(pk["x_all_host"], non_blocking=True)
             self._head(qg)
             self._lm(qg)
-            for p in projs:
-                p["y_host"].copy_(p["y"], non_blocking=True)
+            pk["y_all_host"].copy_(pk["y_all"], non_blocking=True)
         torch.cuda.synchronize()
 
     def _head(self, qg):
@@ -237,17 +250,6 @@ class DecodeGraphs:
 
     def step_e2e(self, timer=None):
         self.g_e2e.replay()
-
-
-def decode_step(projs, timer=None):
-    import block_quantized_integer_gb300 as qg
-    for j, p in enumerate(projs):
-        qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
-        if timer is not None and j == len(projs) - 1:
-            timer[0].record()
-        qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
-        if timer is not None and j == len(projs) - 1:
-            timer[1].record()
 
 
 def max_over_ranks(ms, dist=None, device="cuda"):
@@ -666,8 +668,8 @@ def main():
     # end to end: pinned host x in, y out, every step
     ms_e2e, _ = timed(graphs.step_e2e, max(args.steps // 4, 10), 3, dist)
     e2e = replica_value(world, bytes_step, max(args.steps // 4, 10), ms_e2e)
-    h2d = sum(p["x_host"].numel() * 4 for p in projs)
-    d2h = sum(p["y_host"].numel() * 4 for p in projs)
+    h2d = projs[0]["x_all_host"].numel() * 4
+    d2h = projs[0]["y_all_host"].numel() * 4
 
     N_lm, K_lm = shapes[-1]
     lm_bytes = decode_bytes(1, [(N_lm, K_lm)])
