@@ -449,34 +449,44 @@ def moe_layer_section(dev, peaks, reps=20):
 
 
 def decode_shapes_section(dev, peaks, reps=50):
-    """Each decode projection on its own (activation quantization + GEMV, the two
-    launches of one projection) at M = 1 and M = 4, L2 flushed before every timed
-    call (the 17.8 MB projection would otherwise be served from L2); median of reps."""
+    """Each decode projection on its own at M = 1 and M = 4, L2 flushed before every
+    timed call (the 17.8 MB projection would otherwise be served from L2); median of
+    reps.  Keys M{M}_{N}x{K}: activation quantization + GEMV, two launches;
+    fused_M{M}_{N}x{K}: the one-launch GEMV that quantizes x itself."""
     import torch
     import block_quantized_integer_gb300 as qg
     scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
     out = {}
+
+    def median_ms(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            scrub.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
     for M in (1, 4):
         projs = make_decode(dev, M)
         for p in projs:
-            def one():
+            def two():
                 qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
                 qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
-            for _ in range(3):
-                one()
-            ts = []
-            for _ in range(reps):
-                scrub.fill_(1.0)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                one()
-                b.record()
-                torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
-            ms = statistics.median(ts)
+
+            def fused():
+                qg.qgemv_q8_0_f32(p["x"], p["qw"], p["dw"], y=p["y"])
             nb = decode_bytes(M, [(p["N"], p["K"])])
-            out[f"M{M}_{p['N']}x{p['K']}"] = {"us": ms * 1e3, "gbs": nb / (ms * 1e-3) / 1e9,
-                                              "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            for key, fn in ((f"M{M}_{p['N']}x{p['K']}", two),
+                            (f"fused_M{M}_{p['N']}x{p['K']}", fused)):
+                ms = median_ms(fn)
+                out[key] = {"us": ms * 1e3, "gbs": nb / (ms * 1e-3) / 1e9,
+                            "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del projs
         torch.cuda.empty_cache()
     out["l2"] = "flushed before every timed call"

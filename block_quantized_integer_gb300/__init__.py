@@ -25,7 +25,7 @@ from ._native import QGError
 __all__ = [
     "QGError", "ALGO_AUTO", "ALGO_GEMV", "ALGO_MMA", "ALGO_TCGEN05",
     "quantize_act_q8", "quantize_weight_q8_0", "quantize_weight_q4_0",
-    "qgemm_q8_0", "qgemm_q4_0", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
+    "qgemm_q8_0", "qgemm_q4_0", "qgemv_q8_0_f32", "moe_route", "grouped_qgemm_moe", "grouped_qgemm_moe_noalloc",
     "import_gguf_q8_0", "import_gguf_q4_0",
     "attn_splitk_merge", "kv3_encode", "kv3_decode", "kv3_codebook",
     "moe_swiglu_quant", "moe_combine",
@@ -137,6 +137,27 @@ def _dense(name, qx, dx, qw, dw, y, algo, workspace, wdtype, kfac):
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _native.call(name, _ptr(qx), _ptr(dx), M, N, K, _ptr(qw), _ptr(dw), _ptr(y), y.stride(0),
                  ws_ptr, ws_bytes, int(algo), _stream(dev))
+    return y
+
+
+def qgemv_q8_0_f32(x, qw, dw, y=None):
+    """Decode product from binary32 activations x [M, K] (M <= 8, rows may be
+    strided): the activation quantization runs inside the GEMV; y equals
+    qgemm_q8_0(*quantize_act_q8(x), qw, dw) bit for bit."""
+    _need(x, torch.float32, "x", rows_strided=True)
+    dev = x.device
+    _need(qw, torch.int8, "qw", dev)
+    _need(dw, torch.float16, "dw", dev)
+    M, K = x.shape
+    N = qw.shape[0]
+    if qw.shape[1] != K or dw.shape != (N, K // 32):
+        raise ValueError("shape mismatch between x/qw/dw")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    elif y.dtype != torch.float32 or y.device != dev or y.stride(1) != 1 or tuple(y.shape) != (M, N):
+        raise ValueError("y must be float32 [M, N] on the same device with unit column stride")
+    _native.call("qgemv_q8_0_f32", _ptr(x), M, K, x.stride(0), _ptr(qw), _ptr(dw), N, _ptr(y),
+                 y.stride(0), _stream(dev))
     return y
 
 

@@ -30,6 +30,7 @@ SIGNATURES = {
     "quantize_weight_q4_0": (ctypes.c_int, [P, I64, I64, P, P, P]),
     "qgemm_q8_0": (ctypes.c_int, [P, P, I64, I64, I64, P, P, P, I64, P, SZ, P]),
     "qgemm_q4_0": (ctypes.c_int, [P, P, I64, I64, I64, P, P, P, I64, P, SZ, P]),
+    "qgemv_q8_0_f32": (ctypes.c_int, [P, I64, I64, I64, P, P, I64, P, I64, P]),
     "qgemm_q8_0_ex": (ctypes.c_int, [P, P, I64, I64, I64, P, P, P, I64, P, SZ, ctypes.c_int, P]),
     "qgemm_q4_0_ex": (ctypes.c_int, [P, P, I64, I64, I64, P, P, P, I64, P, SZ, ctypes.c_int, P]),
     "moe_route": (ctypes.c_int, [P, I64, I32, I32, P, P, P, P, P]),

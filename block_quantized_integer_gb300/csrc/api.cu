@@ -201,6 +201,17 @@ qg_status qgemm_q8_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, in
                  QG_ALGO_AUTO, stream);
 }
 
+qg_status qgemv_q8_0_f32(const float* x, int64_t M, int64_t K, int64_t ldx, const int8_t* qw,
+                         const uint16_t* dw, int64_t N, float* y, int64_t ldy, cudaStream_t stream) {
+    if (M < 0 || M > 8 || N <= 0 || K <= 0 || K % kGroup != 0) return QG_ERR_INVALID_ARG;
+    if (M == 0) return QG_OK;
+    if (!x || !qw || !dw || !y || ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (((uintptr_t)x & 3u) || !aligned16(qw) || ((uintptr_t)y & 3u) || ((uintptr_t)dw & 1u))
+        return QG_ERR_ALIGNMENT;
+    if (M * K + (M * K) / 8 > (int64_t)200 * 1024) return QG_ERR_UNSUPPORTED;
+    return from_cuda(qg::launch_gemv_fx(x, ldx, M, N, K, qw, dw, y, ldy, stream));
+}
+
 qg_status qgemm_q4_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                      const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -196,6 +196,183 @@ gemv_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
     }
 }
 
+// ---- activation quantization fused into the GEMV (binary32 x in) ---------------
+//
+// y = (Q8 weights) x quant(x) with quant the activation rule of
+// quantize_act_q8, bit for bit: one resident wave of persistent blocks, each
+// first quantizing all M x K activations into shared memory (8 threads per
+// group, max|x| by shuffles, d = max / 127 and every code by IEEE binary32
+// division, round-half-even, clamp), then walking row tiles b, b + grid, ...
+// with the arithmetic and summation order of gemv_kernel (Q8, 4 rows a warp,
+// W K-slices a row set).  One launch instead of two, at the price of every
+// block reading and quantizing the whole of x before its first weight load.
+__device__ __forceinline__ int quant_code(float v, float d) {
+    if (d == 0.0f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(v, d));
+    return min(max(q, -127), 127);
+}
+
+template <int M, int R, int W>
+__global__ void __launch_bounds__(256, M == 1 ? 3 : 2)
+gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8_t* __restrict__ qw,
+               const uint16_t* __restrict__ dw, float* __restrict__ y, int64_t N, int64_t K,
+               int64_t ldy, int64_t tiles) {
+    constexpr int SETS = kWarps / W;
+    extern __shared__ __align__(16) uint8_t fx_smem[];  // codes [M][K], then scales [M][G]
+    __shared__ float part[kWarps][R][M];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = K / kGroup;
+    int8_t* sq = reinterpret_cast<int8_t*>(fx_smem);
+    float* sd = reinterpret_cast<float*>(fx_smem + ((M * K + 15) & ~(int64_t)15));
+    pdl_wait();                               // x and the weights may come from the previous kernel
+    // quantize: 8 threads per group, 32 groups per pass and U passes' loads in
+    // flight together (the full warp runs every pass)
+    constexpr int U = 4;
+    const int sub = threadIdx.x & 7;
+    const int64_t per_pass = blockDim.x / 8;
+    for (int64_t base = 0; base < M * G; base += U * per_pass) {
+        float4 v[U];
+        int64_t grp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            grp[u] = base + u * per_pass + (threadIdx.x >> 3);
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (grp[u] < M * G) {
+                const int64_t m = grp[u] / G, g = grp[u] % G;
+                const float* p = x + m * ldx + g * kGroup + sub * 4;
+                v[u] = vec_x ? *reinterpret_cast<const float4*>(p) : make_float4(p[0], p[1], p[2], p[3]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const float d = __fdiv_rn(a, 127.0f);
+            if (grp[u] < M * G) {
+                // codes [M][K] and scales [M][G] row-major: the flat group index
+                const uint32_t packed = (uint32_t)(quant_code(v[u].x, d) & 0xff) |
+                                        ((uint32_t)(quant_code(v[u].y, d) & 0xff) << 8) |
+                                        ((uint32_t)(quant_code(v[u].z, d) & 0xff) << 16) |
+                                        ((uint32_t)(quant_code(v[u].w, d) & 0xff) << 24);
+                *reinterpret_cast<uint32_t*>(sq + grp[u] * kGroup + sub * 4) = packed;
+                if (sub == 0) sd[grp[u]] = d;
+            }
+        }
+    }
+    __syncthreads();
+    const int split = warp % W;
+    const int64_t gps = (G + W - 1) / W;
+    const int64_t g0 = split * gps, g1 = min64(G, g0 + gps);
+    const int64_t b0 = g0 * kGroup, b1 = g1 * kGroup;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t n0 = (tile * SETS + warp / W) * R;
+        float acc[R][M];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+        if (n0 < N) {
+            const uint8_t* rowp[R];
+            bool rok[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                rok[r] = n0 + r < N;
+                rowp[r] = qw + (rok[r] ? n0 + r : n0) * K;
+            }
+            for (int64_t base = b0; base < b1; base += 512) {
+                const int64_t off = base + lane * 16;
+                const bool ok = off < b1;             // same for both lanes of a group
+                uint4 wv[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    wv[r] = (ok && rok[r]) ? ldg_nc_v4(rowp[r] + off) : make_uint4(0, 0, 0, 0);
+                const int64_t g = off / kGroup;
+                float dwf[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) dwf[r] = (ok && rok[r]) ? half_bits_to_float(dw[(n0 + r) * G + g]) : 0.f;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const uint4 xv = ok ? *reinterpret_cast<const uint4*>(sq + m * K + off) : make_uint4(0, 0, 0, 0);
+                    const float dxm = ok ? sd[m * G + g] : 0.f;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        int s = dp4a_ss(wv[r].x, xv.x, 0);
+                        s = dp4a_ss(wv[r].y, xv.y, s);
+                        s = dp4a_ss(wv[r].z, xv.z, s);
+                        s = dp4a_ss(wv[r].w, xv.w, s);
+                        s += __shfl_xor_sync(0xffffffffu, s, 1);   // exact group sum
+                        if ((lane & 1) == 0) acc[r][m] = fmaf((float)s, dwf[r] * dxm, acc[r][m]);
+                    }
+                }
+            }
+        }
+        if (tile + gridDim.x >= tiles) pdl_release();   // this block's last weight loads are issued
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float v = acc[r][m];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                acc[r][m] = v;
+            }
+        if (W == 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (n0 + r < N) {
+#pragma unroll
+                        for (int m = 0; m < M; ++m) y[m * ldy + n0 + r] = acc[r][m];
+                    }
+            }
+            continue;
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < M; ++m) part[warp][r][m] = acc[r][m];
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < SETS * R * M; i += blockDim.x) {
+            const int set = i / (R * M), r = (i / M) % R, m = i % M;
+            const int64_t n = (tile * SETS + set) * R + r;
+            if (n < N) {
+                float v = part[set * W][r][m];
+#pragma unroll
+                for (int s = 1; s < W; ++s) v += part[set * W + s][r][m];
+                y[m * ldy + n] = v;
+            }
+        }
+        __syncthreads();                      // part is written again for the next tile
+    }
+}
+
+constexpr size_t kFxSmemMax = 200 * 1024;     // codes + scales of x in one block
+
+template <int M, int R, int W>
+cudaError_t launch_fx_w(const float* x, int64_t ldx, const uint8_t* qw, const uint16_t* dw, float* y,
+                        int64_t N, int64_t K, int64_t ldy, cudaStream_t s) {
+    auto kern = gemv_fx_kernel<M, R, W>;
+    const size_t smem = (size_t)(((M * K + 15) & ~(int64_t)15) + 4 * M * (K / kGroup));
+    if (smem > kFxSmemMax) return cudaErrorInvalidValue;
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFxSmemMax);
+    if (attr != cudaSuccess) return attr;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t rows_per_block = (kWarps / W) * R;
+    const int64_t tiles = (N + rows_per_block - 1) / rows_per_block;
+    int64_t grid = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    if (grid > tiles) grid = tiles;
+    const bool vec_x = ((uintptr_t)x & 15u) == 0 && ldx % 4 == 0;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, x, ldx, vec_x, qw, dw, y, N, K,
+                      ldy, tiles);
+}
+
 template <int M, int R, bool kQ4>
 cudaError_t launch_w(int W, const int8_t* qx, const float* dx, const uint8_t* qw,
                      const uint16_t* dw, float* y, int64_t N, int64_t K, int64_t ldy,
@@ -250,6 +427,28 @@ cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N,
         default: return cudaErrorInvalidValue;
     }
 #undef QG_GEMV_CASE
+}
+
+cudaError_t launch_gemv_fx(const float* x, int64_t ldx, int64_t M, int64_t N, int64_t K, const void* qw,
+                           const uint16_t* dw, float* y, int64_t ldy, cudaStream_t s) {
+    const uint8_t* w = (const uint8_t*)qw;
+    const int sm = sm_count();
+#define QG_FX_CASE(MM)                                                                          \
+    case MM: {                                                                                  \
+        constexpr int R = rows_per_warp(MM);                                                    \
+        switch (gemv_split(MM, N, K, false, sm, R)) {                                           \
+            case 1: return launch_fx_w<MM, R, 1>(x, ldx, w, dw, y, N, K, ldy, s);               \
+            case 2: return launch_fx_w<MM, R, 2>(x, ldx, w, dw, y, N, K, ldy, s);               \
+            case 4: return launch_fx_w<MM, R, 4>(x, ldx, w, dw, y, N, K, ldy, s);               \
+            default: return launch_fx_w<MM, R, 8>(x, ldx, w, dw, y, N, K, ldy, s);              \
+        }                                                                                       \
+    }
+    switch (M) {
+        QG_FX_CASE(1) QG_FX_CASE(2) QG_FX_CASE(3) QG_FX_CASE(4)
+        QG_FX_CASE(5) QG_FX_CASE(6) QG_FX_CASE(7) QG_FX_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef QG_FX_CASE
 }
 
 }  // namespace qg

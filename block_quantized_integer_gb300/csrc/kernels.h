@@ -26,6 +26,10 @@ cudaError_t launch_quantize_weight(const float* w, int64_t N, int64_t K, void* q
                                    uint16_t* dw, bool q4, cudaStream_t s);
 
 int gemv_split(int64_t M, int64_t N, int64_t K, bool q4, int sm, int R);
+// Q8 GEMV from binary32 activations quantized in each block (M <= 8);
+// cudaErrorInvalidValue when x's codes and scales exceed a block's shared memory.
+cudaError_t launch_gemv_fx(const float* x, int64_t ldx, int64_t M, int64_t N, int64_t K, const void* qw,
+                           const uint16_t* dw, float* y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                         const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                         cudaStream_t s);

@@ -146,6 +146,17 @@ qg_status qgemm_q8_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, in
                      const int8_t* qw, const uint16_t* dw, float* y, int64_t ldy,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Decode Q8_0 product from binary32 activations, M <= 8 (the activation
+ * quantization moved into the GEMV, one launch instead of quantize_act_q8 +
+ * qgemm_q8_0): x binary32 [M][ldx] (ldx >= K), every block quantizing all of x
+ * into shared memory with quantize_act_q8's rule, then the decode GEMV.  y is
+ * bit for bit what quantize_act_q8 followed by qgemm_q8_0 writes.
+ * QG_ERR_INVALID_ARG for M outside 1..8 (0 is a no-op), QG_ERR_UNSUPPORTED when
+ * M * K * 1.125 bytes exceed 200 KiB (one block's share of x), alignment as
+ * qgemm_q8_0 (x: 4 bytes). */
+qg_status qgemv_q8_0_f32(const float* x, int64_t M, int64_t K, int64_t ldx, const int8_t* qw,
+                         const uint16_t* dw, int64_t N, float* y, int64_t ldy, cudaStream_t stream);
+
 /* Dense Q4_0 x Q8 product: as qgemm_q8_0 with 4-bit weights qw4 [N][K/2]. */
 qg_status qgemm_q4_0(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                      const uint8_t* qw4, const uint16_t* dw, float* y, int64_t ldy,

@@ -66,6 +66,20 @@ def test_dense_validation(lib):
     assert lib.qgemm_q8_0_ex(A, B, 9, 256, 512, C, D, Y, 256, NUL, 0, 77, S) == 1
 
 
+def test_fused_gemv_validation(lib):
+    f = lib.qgemv_q8_0_f32
+    assert f(A, 9, 512, 512, C, D, 256, Y, 256, S) == 1            # M > 8
+    assert f(A, 4, 500, 500, C, D, 256, Y, 256, S) == 1            # K % 32
+    assert f(A, 4, 512, 511, C, D, 256, Y, 256, S) == 1            # ldx < K
+    assert f(A, 4, 512, 512, C, D, 256, Y, 255, S) == 1            # ldy < N
+    assert f(NUL, 4, 512, 512, C, D, 256, Y, 256, S) == 1          # null x
+    assert f(ctypes.c_void_p(0x10002), 4, 512, 512, C, D, 256, Y, 256, S) == 2
+    assert f(A, 4, 512, 512, ctypes.c_void_p(0x30008), D, 256, Y, 256, S) == 2
+    assert f(A, 0, 512, 512, C, D, 256, Y, 256, S) == 0            # M == 0: no-op
+    # 8 rows x 24576: 221 KiB of codes and scales, above one block's share
+    assert f(A, 8, 24576, 24576, C, D, 256, Y, 256, S) == 5
+
+
 def test_quantize_validation(lib):
     assert lib.quantize_act_q8(A, 4, 48, 48, B, C, S) == 1            # K % 32
     assert lib.quantize_act_q8(A, 4, 64, 32, B, C, S) == 1            # ldx < K

@@ -230,6 +230,56 @@ def test_decode_full_shape(decode_weights, shape, M):
     assert_close(to_np(y), y_ref, mag)
 
 
+# ------------------------------------------------------------------ GEMV with the quantization fused
+
+# (M, N, K, x row padding): K-splits W = 1, 2, 4 and 8 among them, a ragged last row
+# tile, and rows padded by 3 floats (not 16-byte aligned: scalar x loads)
+FUSED_SHAPES = [(1, 4096, 4096, 0), (4, 4096, 4096, 0), (1, 300, 12288, 0), (3, 37, 96, 3),
+                (8, 1000, 1024, 0), (2, 33, 12288, 3), (7, 129, 4160, 0), (1, 5, 32, 0),
+                (5, 40000, 512, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,pad", FUSED_SHAPES)
+def test_fused_gemv_equals_two_launches(M, N, K, pad):
+    """qgemv_q8_0_f32(x) writes exactly what quantize_act_q8 + qgemm_q8_0 write, and
+    that is within tolerance of the oracle on the oracle's own codes."""
+    rng = np.random.default_rng(300 + M * 7 + N + K)
+    x = rng.standard_normal((M, K + pad)).astype(np.float32)
+    x[0, :32] = 0.0                                   # an all-zero group: d = 0, codes 0
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qw, dw = qg.quantize_weight_q8_0(to_dev(w))
+    xt = to_dev(x)[:, :K]
+    y_fused = qg.qgemv_q8_0_f32(xt, qw, dw)
+    qx, dx = qg.quantize_act_q8(xt)
+    y_two = qg.qgemm_q8_0(qx, dx, qw, dw)
+    _sync()
+    assert torch.equal(y_fused, y_two)
+    qx_ref, dx_ref = oracle.quantize_act_q8(np.ascontiguousarray(x[:, :K]))
+    qw_ref, dw_ref = oracle.quantize_w_q8_0(w)
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref, dw_ref, 8)
+    assert_close(to_np(y_fused), y_ref, mag)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_fused_gemv_lm_head_full_size(decode_weights, M):
+    """The 151936 x 4096 lm-head projection of the decode workload: the fused call
+    equals the two-launch path bit for bit; sampled rows against the oracle."""
+    shape = inputs.DECODE_SHAPES[-1]
+    w, x, qw_ref, dw_ref = decode_weights[shape]
+    x = x[:M]
+    qw, dw = qg.quantize_weight_q8_0(to_dev(w))
+    xt = to_dev(x)
+    y_fused = qg.qgemv_q8_0_f32(xt, qw, dw)
+    qx, dx = qg.quantize_act_q8(xt)
+    y_two = qg.qgemm_q8_0(qx, dx, qw, dw)
+    _sync()
+    assert torch.equal(y_fused, y_two)
+    rows = np.sort(np.random.default_rng(9).choice(shape[0], 64, replace=False))
+    qx_ref, dx_ref = oracle.quantize_act_q8(x)
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref[rows], dw_ref[rows], 8)
+    assert_close(to_np(y_fused)[:, rows], y_ref, mag)
+
+
 # ------------------------------------------------------------------ full-size prefill (sampled)
 
 @pytest.mark.parametrize("algo", [qg.ALGO_AUTO, qg.ALGO_MMA])
