@@ -57,6 +57,37 @@ def test_quantize_act_golden_ties():
     assert to_np(dx)[0, 0] == 1.0
 
 
+def test_quantize_act_near_ties():
+    """Quotients x / d placed within 1e-6 .. 5e-4 of a half-integer, and on it, where
+    any shortcut past the binary32 division would show first: codes bit-exact with
+    the oracle's, also through the GEMV that quantizes its own activations."""
+    rng = np.random.default_rng(4242)
+    M, K = 128, 1024
+    G = M * K // 32
+    amax = rng.uniform(0.5, 3.0, G).astype(np.float32)
+    d = amax / np.float32(127.0)                       # binary32 quotients, as the rule
+    k = rng.integers(-126, 126, (G, 31)).astype(np.float64)
+    off = rng.choice([-5e-4, -3e-4, -2e-4, -3e-5, -1e-5, -1e-6, 0.0, 1e-6, 1e-5, 3e-5, 2e-4,
+                      3e-4, 5e-4], (G, 31))
+    g = np.empty((G, 32), np.float32)
+    g[:, 0] = amax
+    g[:, 1:] = ((k + 0.5 + off) * d[:, None].astype(np.float64)).astype(np.float32)
+    x = g.reshape(M, K)
+    qx_ref, dx_ref = oracle.quantize_act_q8(x)
+    qx, dx = qg.quantize_act_q8(to_dev(x))
+    _sync()
+    assert np.array_equal(to_np(qx), qx_ref)
+    assert np.array_equal(to_np(dx).view(np.uint32), dx_ref.view(np.uint32))
+    w = (rng.standard_normal((64, K)) * 0.02).astype(np.float32)
+    qw, dw = qg.quantize_weight_q8_0(to_dev(w))
+    for m0 in range(0, M, 8):                          # the fused GEMV, 8 rows at a time
+        xs = to_dev(x[m0:m0 + 8])
+        y_fused = qg.qgemv_q8_0_f32(xs, qw, dw)
+        y_two = qg.qgemm_q8_0(qx[m0:m0 + 8].contiguous(), dx[m0:m0 + 8].contiguous(), qw, dw)
+        _sync()
+        assert torch.equal(y_fused, y_two)
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("N,K", [(256, 512), (300, 96), (7, 32), (1024, 2048)])
 def test_quantize_weight_bit_exact(bits, N, K):
