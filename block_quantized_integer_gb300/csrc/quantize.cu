@@ -12,8 +12,9 @@
 // Built without --use_fast_math and without flush-to-zero, so subnormal
 // scales divide exactly as IEEE says.
 //
-// Layout of the work: 8 threads per group, 4 consecutive elements per thread
-// (one 16-byte load), a warp covers 4 groups = 512 contiguous bytes of input.
+// Layout of the work: activations 4 threads per group with 8 consecutive
+// elements each (two 16-byte loads, a warp covers 8 groups = 1 KiB of input);
+// weights 8 threads per group with 4 elements each (one 16-byte load).
 // HBM-bound: 4 bytes read and 1.125 (activations) / 1.0625 (Q8) / 0.5625 (Q4)
 // bytes written per element.
 #include "common.cuh"
@@ -56,6 +57,9 @@ __device__ __forceinline__ uint16_t scale16(float amax, float qmax) {
 }
 
 // kFast: M * G < 2^32, flat group index split into (row, group) by FastDiv.
+// 4 threads per group, 8 consecutive elements (two 16-byte loads) per thread,
+// U groups per thread with their loads in flight together; a warp covers 8
+// groups = 1 KiB of contiguous input per pass.
 template <bool kFast>
 __global__ void __launch_bounds__(256)
 quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
@@ -63,21 +67,21 @@ quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_
     constexpr int U = 2;                          // groups per thread in flight
     const int64_t G = K / kGroup;
     const int64_t total = M * G;
-    const int sub = threadIdx.x & 7;
-    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 3);
+    const int sub = threadIdx.x & 3;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 2);
     // Every lane of a warp runs the same number of iterations (the shuffles
     // need the full warp), so the loop bound is rounded up to whole warps.
-    const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 3) + (threadIdx.x >> 3);
-    const int64_t warp_first = first - ((threadIdx.x & 31) >> 3);
+    const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 2) + (threadIdx.x >> 2);
+    const int64_t warp_first = first - ((threadIdx.x & 31) >> 2);
     pdl_wait();                               // x may come from the previous kernel
     pdl_release();                            // the next kernel may launch and wait for this one
     for (int64_t base = warp_first; base < total; base += U * stride) {
-        float4 v[U];
+        float4 v[U][2];
         int64_t grp[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {             // all loads first
-            grp[u] = base + u * stride + ((threadIdx.x & 31) >> 3);
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            grp[u] = base + u * stride + ((threadIdx.x & 31) >> 2);
+            v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (grp[u] < total) {
                 int64_t m, g;
                 if constexpr (kFast) {
@@ -87,19 +91,26 @@ quantize_act_q8_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_
                     m = grp[u] / G;
                     g = grp[u] % G;
                 }
-                v[u] = load4(x + m * ldx + g * kGroup + sub * 4, vec_ok);
+                const float* p = x + m * ldx + g * kGroup + sub * 8;
+                v[u][0] = load4(p, vec_ok);
+                v[u][1] = load4(p + 4, vec_ok);
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool active = grp[u] < total;
-            const float a = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-            const float d = __fdiv_rn(amax8(a), 127.0f);
+            float a = fmaxf(fmaxf(fmaxf(fabsf(v[u][0].x), fabsf(v[u][0].y)), fmaxf(fabsf(v[u][0].z), fabsf(v[u][0].w))),
+                            fmaxf(fmaxf(fabsf(v[u][1].x), fabsf(v[u][1].y)), fmaxf(fabsf(v[u][1].z), fabsf(v[u][1].w))));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));    // max over the group's 4 lanes
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const float d = __fdiv_rn(a, 127.0f);
             if (active) {
                 // codes and scales are stored at the flat group index: [M][G] row-major
-                uint32_t packed = pack_s8(quant1(v[u].x, d, -127, 127), quant1(v[u].y, d, -127, 127),
-                                          quant1(v[u].z, d, -127, 127), quant1(v[u].w, d, -127, 127));
-                *reinterpret_cast<uint32_t*>(qx + grp[u] * kGroup + sub * 4) = packed;
+                const uint32_t lo = pack_s8(quant1(v[u][0].x, d, -127, 127), quant1(v[u][0].y, d, -127, 127),
+                                            quant1(v[u][0].z, d, -127, 127), quant1(v[u][0].w, d, -127, 127));
+                const uint32_t hi = pack_s8(quant1(v[u][1].x, d, -127, 127), quant1(v[u][1].y, d, -127, 127),
+                                            quant1(v[u][1].z, d, -127, 127), quant1(v[u][1].w, d, -127, 127));
+                *reinterpret_cast<uint2*>(qx + grp[u] * kGroup + sub * 8) = make_uint2(lo, hi);
                 if (sub == 0) dx[grp[u]] = d;
             }
         }
