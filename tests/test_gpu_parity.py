@@ -261,6 +261,44 @@ def test_decode_full_shape(decode_weights, shape, M):
     assert_close(to_np(y), y_ref, mag)
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_decode_step_as_benchmarked(M):
+    """The decode step exactly as bench.py times it: bench's own buffers and CUDA graphs
+    (the one-graph step with dependent launches, the split graphs, the end-to-end graph
+    with host copies).  Every projection's output equals a direct call of the ABI bit for
+    bit after each replay, and sampled lm-head rows match the oracle."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    projs = bench.make_decode(dev(), M)
+    graphs = bench.DecodeGraphs(projs)
+    ref = []
+    for p in projs:
+        qx, dx = qg.quantize_act_q8(p["x"])
+        ref.append(qg.qgemm_q8_0(qx, dx, p["qw"], p["dw"]))
+    _sync()
+    for replay in (graphs.step_full, graphs.step, graphs.step_e2e):
+        for p in projs:
+            p["y"].fill_(float("nan"))
+        replay()
+        _sync()
+        for p, r in zip(projs, ref):
+            assert torch.equal(p["y"], r)
+    pk = projs[0]
+    host = pk["y_all_host"].clone()
+    assert torch.equal(host.to(dev()), pk["y_all"])          # the end-to-end copy out
+    p = projs[-1]
+    N, K = p["N"], p["K"]
+    w, x = inputs.decode_case(N, K, M=M, sub=len(projs) - 1)
+    qw_ref, dw_ref = oracle.quantize_w_q8_0(w)
+    qx_ref, dx_ref = oracle.quantize_act_q8(x)
+    rows = np.sort(np.random.default_rng(11).choice(N, 64, replace=False))
+    y_ref, mag = oracle.qgemm(qx_ref, dx_ref, qw_ref[rows], dw_ref[rows], 8)
+    assert_close(to_np(p["y"])[:, rows], y_ref, mag)
+    del graphs, projs
+
+
 # ------------------------------------------------------------------ GEMV with the quantization fused
 
 # (M, N, K, x row padding): K-splits W = 1, 2, 4 and 8 among them, a ragged last row
