@@ -228,10 +228,13 @@ class DecodeGraphs:
         torch.cuda.synchronize()
 
     def _head(self, qg):
-        for p in self.projs:
-            qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
+        # projection by projection: quantize, then its GEMV; the lm-head's
+        # quantization closes the head so that its GEMV can stand alone
         for p in self.projs[:-1]:
+            qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
             qg.qgemm_q8_0(p["qx"], p["dx"], p["qw"], p["dw"], y=p["y"])
+        p = self.projs[-1]
+        qg.quantize_act_q8(p["x"], p["qx"], p["dx"])
 
     def _lm(self, qg):
         p = self.projs[-1]
