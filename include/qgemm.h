@@ -53,7 +53,7 @@ typedef enum {
     QG_ERR_ALIGNMENT = 2,    /* a base pointer or leading dimension is misaligned */
     QG_ERR_WORKSPACE = 3,    /* workspace missing or smaller than qgemm_workspace_size() */
     QG_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed */
-    QG_ERR_UNSUPPORTED = 5   /* valid request this build does not handle */
+    QG_ERR_UNSUPPORTED = 5   /* valid request outside what the library handles */
 } qg_status;
 
 /* Kernel choice for the *_ex entry points. QG_ALGO_AUTO picks by shape. */
