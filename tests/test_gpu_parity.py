@@ -438,6 +438,24 @@ def test_moe_route_invalid_ids():
     assert np.array_equal(to_np(p)[: offsets[6]], perm)
 
 
+def test_moe_empty_batch():
+    """No tokens: routing writes all-zero counts and offsets, the grouped product returns
+    an empty output and flags nothing."""
+    ids = torch.empty((0, 8), dtype=torch.int32, device=dev())
+    c, o, p, d_err = qg.moe_route(ids, 16)
+    _sync()
+    assert np.all(to_np(c) == 0) and np.all(to_np(o) == 0) and int(to_np(d_err)[0]) == 0
+    E, N, K = 4, 64, 256
+    qw4 = torch.zeros((E, N, K // 2), dtype=torch.uint8, device=dev())
+    dw = torch.zeros((E, N, K // 32), dtype=torch.float16, device=dev())
+    qx = torch.zeros((0, K), dtype=torch.int8, device=dev())
+    dx = torch.zeros((0, K // 32), dtype=torch.float32, device=dev())
+    y, err = qg.grouped_qgemm_moe(qx, dx, torch.empty((0, 2), dtype=torch.int32, device=dev()),
+                                  0, qw4, dw)
+    _sync()
+    assert y.shape == (0, N) and int(to_np(err)[0]) == 0 and qg.device_error() == 0
+
+
 @pytest.mark.parametrize("K", [128, 512])      # K % 256 == 0 takes the tensor-core kernel
 @pytest.mark.parametrize("mode", [0, 1])
 def test_grouped_moe_small(mode, K):
