@@ -240,7 +240,7 @@ qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                     cudaStream_t stream) {
     if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || T * (int64_t)topk >= (1ll << 31))
         return QG_ERR_INVALID_ARG;
-    if (!topk_ids || !counts || !offsets || !perm || !d_err) return QG_ERR_INVALID_ARG;
+    if ((T > 0 && !topk_ids) || !counts || !offsets || !perm || !d_err) return QG_ERR_INVALID_ARG;
     if (((uintptr_t)topk_ids | (uintptr_t)counts | (uintptr_t)offsets | (uintptr_t)perm |
          (uintptr_t)d_err) & 3u)
         return QG_ERR_ALIGNMENT;

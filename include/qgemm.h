@@ -181,7 +181,8 @@ qg_status qgemm_q4_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N,
  *   perm [T*topk] pair indices grouped by expert, (token, slot) order inside
  *                 an expert; entries past offsets[E] are left unspecified.
  * Ids outside [0, E) are not routed: *d_err (device int32) is incremented once
- * per such pair and nothing traps.  Deterministic.  E <= 1024, T*topk < 2^31. */
+ * per such pair and nothing traps.  Deterministic.  E <= 1024, T*topk < 2^31.
+ * T = 0 is valid (topk_ids may then be NULL): counts and offsets are zeroed. */
 qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* d_err,
                     cudaStream_t stream);

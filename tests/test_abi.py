@@ -105,6 +105,7 @@ def test_moe_validation_and_workspace(lib):
     assert g(A, B, 947, 2048, C, 947, 8, 2, D, E, 128, 2048, Y, C, W, ws, S) == 1
     assert g(A, B, 947, 2048, C, 947, 8, 0, D, E, 2000, 2048, Y, C, W, ws, S) == 1  # E > 1024
     assert lib.moe_route(A, 10, 2, 2000, B, C, D, Y, S) == 1
+    assert lib.moe_route(NUL, 10, 2, 16, B, C, D, Y, S) == 1     # null ids with T > 0
     assert g(A, B, 0, 2048, C, 0, 8, 0, D, E, 128, 2048, Y, C, W, ws, S) == 0   # T == 0: no-op
 
 
