@@ -212,9 +212,14 @@ __device__ __forceinline__ int quant_code(float v, float d) {
     return min(max(q, -127), 127);
 }
 
-template <int M, int R, int W>
+// kPre: the activations arrive quantized (qx int8 [M][K] in x8, dx [M][G] in
+// xd) and are only copied into shared memory; else x holds binary32 [M][ldx].
+// kWhole: a lane takes a whole group of each row (see gemv_rows_whole); else
+// the half-group layout and arithmetic order of gemv_kernel.
+template <int M, int R, int W, bool kPre, bool kWhole>
 __global__ void __launch_bounds__(256, M == 1 ? 3 : 2)
-gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8_t* __restrict__ qw,
+gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const int8_t* __restrict__ x8,
+               const float* __restrict__ xd, const uint8_t* __restrict__ qw,
                const uint16_t* __restrict__ dw, float* __restrict__ y, int64_t N, int64_t K,
                int64_t ldy, int64_t tiles) {
     constexpr int SETS = kWarps / W;
@@ -225,6 +230,24 @@ gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8
     int8_t* sq = reinterpret_cast<int8_t*>(fx_smem);
     float* sd = reinterpret_cast<float*>(fx_smem + ((M * K + 15) & ~(int64_t)15));
     pdl_wait();                               // x and the weights may come from the previous kernel
+    if constexpr (kPre) {
+        // copy the codes (16 bytes a thread, four loads in flight) and the scales
+        const int64_t n16 = M * K / 16;
+        for (int64_t i0 = threadIdx.x; i0 < n16; i0 += 4 * (int64_t)blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * (int64_t)blockDim.x;
+                if (i < n16) v[u] = ldg_v4(x8 + 16 * i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * (int64_t)blockDim.x;
+                if (i < n16) reinterpret_cast<uint4*>(sq)[i] = v[u];
+            }
+        }
+        for (int64_t i = threadIdx.x; i < M * G; i += blockDim.x) sd[i] = xd[i];
+    } else {
     // quantize: 8 threads per group, 32 groups per pass and U passes' loads in
     // flight together (the full warp runs every pass)
     constexpr int U = 4;
@@ -261,6 +284,7 @@ gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8
             }
         }
     }
+    }
     __syncthreads();
     const int split = warp % W;
     const int64_t gps = (G + W - 1) / W;
@@ -281,6 +305,43 @@ gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8
                 rok[r] = n0 + r < N;
                 rowp[r] = qw + (rok[r] ? n0 + r : n0) * K;
             }
+            if constexpr (kWhole) {
+                // a lane holds one whole group (32 bytes) of each row, a step covers 32
+                // groups: the group sum is 8 dp4a in one lane, with no shuffle
+                for (int64_t gb = g0; gb < g1; gb += 32) {
+                    const int64_t g = gb + lane;
+                    const bool ok = g < g1;
+                    uint4 wa[R], wb[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const bool v = ok && rok[r];
+                        wa[r] = v ? ldg_nc_v4(rowp[r] + g * kGroup) : make_uint4(0, 0, 0, 0);
+                        wb[r] = v ? ldg_nc_v4(rowp[r] + g * kGroup + 16) : make_uint4(0, 0, 0, 0);
+                    }
+                    float dwf[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        dwf[r] = (ok && rok[r]) ? half_bits_to_float(dw[(n0 + r) * G + g]) : 0.f;
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const uint4 xa = ok ? *reinterpret_cast<const uint4*>(sq + m * K + g * kGroup) : make_uint4(0, 0, 0, 0);
+                        const uint4 xb = ok ? *reinterpret_cast<const uint4*>(sq + m * K + g * kGroup + 16) : make_uint4(0, 0, 0, 0);
+                        const float dxm = ok ? sd[m * G + g] : 0.f;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            int s = dp4a_ss(wa[r].x, xa.x, 0);
+                            s = dp4a_ss(wa[r].y, xa.y, s);
+                            s = dp4a_ss(wa[r].z, xa.z, s);
+                            s = dp4a_ss(wa[r].w, xa.w, s);
+                            s = dp4a_ss(wb[r].x, xb.x, s);
+                            s = dp4a_ss(wb[r].y, xb.y, s);
+                            s = dp4a_ss(wb[r].z, xb.z, s);
+                            s = dp4a_ss(wb[r].w, xb.w, s);       // exact group sum
+                            acc[r][m] = fmaf((float)s, dwf[r] * dxm, acc[r][m]);
+                        }
+                    }
+                }
+            } else
             for (int64_t base = b0; base < b1; base += 512) {
                 const int64_t off = base + lane * 16;
                 const bool ok = off < b1;             // same for both lanes of a group
@@ -352,10 +413,11 @@ gemv_fx_kernel(const float* __restrict__ x, int64_t ldx, bool vec_x, const uint8
 
 constexpr size_t kFxSmemMax = 200 * 1024;     // codes + scales of x in one block
 
-template <int M, int R, int W>
-cudaError_t launch_fx_w(const float* x, int64_t ldx, const uint8_t* qw, const uint16_t* dw, float* y,
-                        int64_t N, int64_t K, int64_t ldy, cudaStream_t s) {
-    auto kern = gemv_fx_kernel<M, R, W>;
+template <int M, int R, int W, bool kPre, bool kWhole>
+cudaError_t launch_fx_w(const float* x, int64_t ldx, const int8_t* x8, const float* xd,
+                        const uint8_t* qw, const uint16_t* dw, float* y, int64_t N, int64_t K,
+                        int64_t ldy, cudaStream_t s) {
+    auto kern = gemv_fx_kernel<M, R, W, kPre, kWhole>;
     const size_t smem = (size_t)(((M * K + 15) & ~(int64_t)15) + 4 * M * (K / kGroup));
     if (smem > kFxSmemMax) return cudaErrorInvalidValue;
     static const cudaError_t attr =
@@ -369,8 +431,8 @@ cudaError_t launch_fx_w(const float* x, int64_t ldx, const uint8_t* qw, const ui
     int64_t grid = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
     if (grid > tiles) grid = tiles;
     const bool vec_x = ((uintptr_t)x & 15u) == 0 && ldx % 4 == 0;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, x, ldx, vec_x, qw, dw, y, N, K,
-                      ldy, tiles);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, x, ldx, vec_x, x8, xd, qw, dw, y,
+                      N, K, ldy, tiles);
 }
 
 template <int M, int R, bool kQ4>
@@ -409,15 +471,46 @@ int gemv_split(int64_t M, int64_t N, int64_t K, bool q4, int sm, int R) {
     return W;
 }
 
+namespace {
+
+// Whether a Q8 product takes a whole group per lane: M >= 2 and at least 8192
+// rows (fewer do not amortize each block's staging of the activations: 4096 x
+// 4096 and 4096 x 12288 at M = 4 ran 1-3 us slower).  The two-launch path and
+// the GEMV that quantizes its own activations follow the same rule, so their
+// results stay bit-identical.
+bool gemv_rows_whole(int64_t M, int64_t N) { return M >= 2 && N >= 8192; }
+
+// Q8 at M >= 2 on large N: the persistent kernel that stages the quantized
+// activations once per block in shared memory and takes a whole group per lane
+// (gemv_fx_kernel with kPre).  At M >= 2 the register-fed kernel below is bound
+// by instruction issue (the half-group shuffles and the activation loads of
+// every step); the M = 4 lm-head ran 155 -> 135 us this way.
+template <int MM, int R>
+cudaError_t launch_pre(int W, const int8_t* qx, const float* dx, const uint8_t* w, const uint16_t* dw,
+                       float* y, int64_t N, int64_t K, int64_t ldy, cudaStream_t s) {
+    switch (W) {
+        case 1: return launch_fx_w<MM, R, 1, true, true>(nullptr, 0, qx, dx, w, dw, y, N, K, ldy, s);
+        case 2: return launch_fx_w<MM, R, 2, true, true>(nullptr, 0, qx, dx, w, dw, y, N, K, ldy, s);
+        case 4: return launch_fx_w<MM, R, 4, true, true>(nullptr, 0, qx, dx, w, dw, y, N, K, ldy, s);
+        default: return launch_fx_w<MM, R, 8, true, true>(nullptr, 0, qx, dx, w, dw, y, N, K, ldy, s);
+    }
+}
+
+}  // namespace
+
 cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                         const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                         cudaStream_t s) {
     const uint8_t* w = (const uint8_t*)qw;
     const int sm = sm_count();
+    const bool staged = !q4 && gemv_rows_whole(M, N) && (size_t)(M * K + M * K / 8) <= kFxSmemMax;
 #define QG_GEMV_CASE(MM)                                                                        \
     case MM: {                                                                                  \
         constexpr int R = rows_per_warp(MM);                                                    \
         const int W = gemv_split(MM, N, K, q4, sm, R);                                          \
+        if constexpr (MM >= 2) {                                                                \
+            if (staged) return launch_pre<MM, R>(W, qx, dx, w, dw, y, N, K, ldy, s);            \
+        }                                                                                       \
         return q4 ? launch_w<MM, R, true>(W, qx, dx, w, dw, y, N, K, ldy, s)                    \
                   : launch_w<MM, R, false>(W, qx, dx, w, dw, y, N, K, ldy, s);                  \
     }
@@ -429,18 +522,32 @@ cudaError_t launch_gemv(const int8_t* qx, const float* dx, int64_t M, int64_t N,
 #undef QG_GEMV_CASE
 }
 
+namespace {
+
+template <int MM, int R, int W>
+cudaError_t launch_fx(bool whole, const float* x, int64_t ldx, const uint8_t* w, const uint16_t* dw,
+                      float* y, int64_t N, int64_t K, int64_t ldy, cudaStream_t s) {
+    if constexpr (MM >= 2) {
+        if (whole) return launch_fx_w<MM, R, W, false, true>(x, ldx, nullptr, nullptr, w, dw, y, N, K, ldy, s);
+    }
+    return launch_fx_w<MM, R, W, false, false>(x, ldx, nullptr, nullptr, w, dw, y, N, K, ldy, s);
+}
+
+}  // namespace
+
 cudaError_t launch_gemv_fx(const float* x, int64_t ldx, int64_t M, int64_t N, int64_t K, const void* qw,
                            const uint16_t* dw, float* y, int64_t ldy, cudaStream_t s) {
     const uint8_t* w = (const uint8_t*)qw;
     const int sm = sm_count();
+    const bool whole = gemv_rows_whole(M, N);
 #define QG_FX_CASE(MM)                                                                          \
     case MM: {                                                                                  \
         constexpr int R = rows_per_warp(MM);                                                    \
         switch (gemv_split(MM, N, K, false, sm, R)) {                                           \
-            case 1: return launch_fx_w<MM, R, 1>(x, ldx, w, dw, y, N, K, ldy, s);               \
-            case 2: return launch_fx_w<MM, R, 2>(x, ldx, w, dw, y, N, K, ldy, s);               \
-            case 4: return launch_fx_w<MM, R, 4>(x, ldx, w, dw, y, N, K, ldy, s);               \
-            default: return launch_fx_w<MM, R, 8>(x, ldx, w, dw, y, N, K, ldy, s);              \
+            case 1: return launch_fx<MM, R, 1>(whole, x, ldx, w, dw, y, N, K, ldy, s);           \
+            case 2: return launch_fx<MM, R, 2>(whole, x, ldx, w, dw, y, N, K, ldy, s);           \
+            case 4: return launch_fx<MM, R, 4>(whole, x, ldx, w, dw, y, N, K, ldy, s);           \
+            default: return launch_fx<MM, R, 8>(whole, x, ldx, w, dw, y, N, K, ldy, s);          \
         }                                                                                       \
     }
     switch (M) {
