@@ -20,6 +20,17 @@
 //     accumulators stay in binary32 (the mining-card page's split-K
 //     FlashAttention section: half-precision partials drifted, binary32 ones
 //     did not).
+// Two kernels implement this:
+//   gemv_kernel     one block per row tile, activations read from global
+//                   memory (through L1); every shape at M = 1, Q4, and Q8 at
+//                   M >= 2 below 8192 rows;
+//   gemv_fx_kernel  one resident wave of persistent blocks, each staging the
+//                   whole activation (its codes and scales, or the binary32 x
+//                   it quantizes itself) in shared memory before walking its
+//                   row tiles; Q8 at M >= 2 from 8192 rows takes a whole group
+//                   per lane there (8 dp4a, no shuffle).  It also serves
+//                   qgemv_q8_0_f32, with the same layout rule, so both entry
+//                   points give the same bits.
 #include "common.cuh"
 #include "kernels.h"
 
