@@ -31,6 +31,10 @@
 //   warps 0-15  epilogue: 16-lane x 256-bit TMEM reads, the pair slot is
 //               released as soon as it is read, then y += (S * dw) * dx on
 //               packed f32x2 instructions into binary32 registers.
+// Dense tail split: when the tile count leaves the grid's last round partly
+// empty, those last tiles are cut along K into chunks (multiples of 8 groups)
+// that fill the round; each chunk stores binary32 partial sums and a small
+// kernel adds each tile's chunks in chunk order.
 // Every mbarrier wait is bounded; on a timeout the CTA sets a device error
 // word, drains its own TMA copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -254,6 +258,40 @@ __device__ __forceinline__ Tile tile_at(int64_t t, int64_t M, int G, const Group
     return T;
 }
 
+// Dense work units.  Units [0, full) are whole output tiles.  When the tile
+// count leaves the last round of the persistent grid partly empty, each of
+// those last tiles is cut along K into `split` chunks of equal length (a
+// multiple of 8 groups, so every stage boundary stays where it was): unit
+// full + l * split + c is chunk c of tile full + l.  A chunk's binary32 sums go
+// to partial slot l * split + c of `part` (BM x BN each), and
+// tail_reduce_kernel adds a tile's chunks in chunk order into y.
+struct TailArgs {
+    int full;          // whole-tile units
+    int split;         // K chunks per tail tile (1: no tail split)
+    float* part;       // [(units - full)][BM][BN] binary32
+};
+
+struct Unit {
+    int tile, g0, pairs, slot;    // output tile, first group, pairs of groups, partial slot (-1: y)
+};
+
+__device__ __forceinline__ Unit unit_at(int t, int PAIRS, const TailArgs& ta) {
+    Unit u;
+    if (t < ta.full) {
+        u.tile = t;
+        u.g0 = 0;
+        u.pairs = PAIRS;
+        u.slot = -1;
+    } else {
+        const int v = t - ta.full;
+        u.pairs = PAIRS / ta.split;
+        u.tile = ta.full + v / ta.split;
+        u.g0 = 2 * u.pairs * (v % ta.split);
+        u.slot = v;
+    }
+    return u;
+}
+
 // Columns a MoE tile's pair slot gives each of its two groups: the tile's
 // rows rounded up to 32, 64 or 128 (the MMA N is the rows rounded up to 16).
 __device__ __forceinline__ int slot_width(int rows) { return rows <= 32 ? 32 : (rows <= 64 ? 64 : BN); }
@@ -396,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
                float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec2,
-               GroupedArgs ga, int n_tiles, int64_t dense_tiles) {
+               GroupedArgs ga, int n_tiles, int64_t dense_tiles, TailArgs ta) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -453,9 +491,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             int64_t ia = 0, ib = 0, isc = 0;      // stages issued so far (run on across tiles)
             bool ok = true;
             for (int t = t0; t < num_tiles && ok; t += dt) {
-                const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
+                int tile = t, gb = 0, ge = G;
+                if constexpr (!kGrouped) {
+                    const Unit u = unit_at(t, PAIRS, ta);
+                    tile = u.tile;
+                    gb = u.g0;
+                    ge = u.g0 + 2 * u.pairs;
+                }
+                const Tile T = tile_at<kGrouped>(tile, M, G, ga, n_tiles);
                 // issue in the order the stages are first needed
-                for (int g = 0; g < G && ok; ++g) {
+                for (int g = gb; g < ge && ok; ++g) {
                     if (g % SCG == 0) {
                         const int slot = (int)(isc % NSC);
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
@@ -559,7 +604,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 }
             } else {
                 for (int t = t0; t < num_tiles && ok; t += dt) {
-                    for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                    const int np = unit_at(t, PAIRS, ta).pairs;
+                    for (int pl = 0; pl < np; ++pl, ++p) {
                         const int so = (int)(p % NO), ps = (int)(p % NP);
                         const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
                         // both probes go out back to back; one branch on the pair
@@ -597,7 +643,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         uint32_t p = 0, sb = 0;                             // run on across tiles
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
-            for (int pl = 0; pl < PAIRS && ok; ++pl, ++p) {
+            const int np = kGrouped ? PAIRS : unit_at(t, PAIRS, ta).pairs;
+            for (int pl = 0; pl < np && ok; ++pl, ++p) {
                 const int g0 = 2 * pl;
                 if (g0 % GB == 0 && !(ok = wait_bar<true>(B.full_b + 8 * (sb % NB), (sb / NB) & 1, abort))) break;
                 // the operand slot is free once the MMAs of pair p - NO completed
@@ -658,14 +705,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             for (int t = t0; t < num_tiles && ok; t += dt) {
                 // a warp with no valid output (ragged last tile) keeps the
                 // barrier protocol but skips the readout and math
-                const int trows = (int)tile_at<kGrouped>(t, M, G, ga, n_tiles).rows;
+                const Unit u = unit_at(t, PAIRS, ta);
+                const int trows = (int)tile_at<kGrouped>(u.tile, M, G, ga, n_tiles).rows;
                 const bool live = q * 32 < trows;
                 uint64_t acc[4][4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
-                for (int pl = 0; pl < PAIRS; ++pl, ++p) {
+                for (int pl = 0; pl < u.pairs; ++pl, ++p) {
                     const int g0 = 2 * pl, ps = (int)(p % NP), so = (int)(p % NO);
                     const int slot = (int)(sc % NSC);
                     if (g0 % SCG == 0 && !(ok = wait_bar<true>(B.full_sc + 8 * slot, (sc / NSC) & 1, abort))) break;
@@ -724,19 +772,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 }
                 if (!ok) break;
                 if (live) {
-                    const Tile T = tile_at<kGrouped>(t, M, G, ga, n_tiles);
+                    const Unit uu = unit_at(t, PAIRS, ta);                 // again: fewer live registers
+                    const Tile T = tile_at<kGrouped>(uu.tile, M, G, ga, n_tiles);
                     {
+                        // a tail chunk stores into its partial slot (BN columns, 8-byte aligned)
+                        const bool part = uu.slot >= 0;
+                        float* ybase = part ? ta.part + (int64_t)uu.slot * (BM * BN) + cb + c2
+                                            : y + T.m0 * ldy + T.n0 + cb + c2;
+                        const int64_t ld = part ? BN : ldy;
+                        const bool v2 = vec2 || part;
                         const int64_t col0 = T.n0 + cb + c2;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int row = rb + 8 * i;                   // tile row
                             if (row < T.rows) {
-                                float* yr = y + (T.m0 + row) * ldy + col0;
+                                float* yr = ybase + row * ld;
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
                                     const float2 v = unpack2(acc[i][j]);
                                     const int64_t col = col0 + 8 * j;
-                                    if (vec2 && col + 1 < N) {
+                                    if (v2 && col + 1 < N) {
                                         *reinterpret_cast<float2*>(yr + 8 * j) = v;
                                     } else {
                                         if (col < N) yr[8 * j] = v.x;
@@ -807,6 +862,27 @@ transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t
         const int r = (int)(sidx & 31), c = r >> 3, j = (r >> 1) & 3, el = r & 1;
         const int64_t n = (sidx & ~(int64_t)31) + 8 * j + 2 * c + el;
         dwt[eg * ldt + sidx] = n < rows_n ? half_bits_to_float(dw[(e * rows_n + n) * G + g]) : 0.f;
+    }
+}
+
+// y of the tail tiles: the sum of each tile's K-chunk partials, added in chunk
+// order (deterministic).  One thread per output element of the tail tiles.
+__global__ void __launch_bounds__(256)
+tail_reduce_kernel(const float* __restrict__ part, int full, int split, int tail_tiles,
+                   int n_tiles, int64_t M, int64_t N, float* __restrict__ y, int64_t ldy) {
+    const int64_t total = (int64_t)tail_tiles * BM * BN;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int l = (int)(i / (BM * BN));
+        const int r = (int)(i / BN) % BM, c = (int)(i % BN);
+        const int tile = full + l;
+        const int64_t m = (int64_t)(tile / n_tiles) * BM + r, n = (int64_t)(tile % n_tiles) * BN + c;
+        if (m < M && n < N) {
+            const float* p = part + (int64_t)l * split * (BM * BN) + r * BN + c;
+            float s = p[0];
+            for (int k = 1; k < split; ++k) s += p[(int64_t)k * (BM * BN)];
+            y[m * ldy + n] = s;
+        }
     }
 }
 
@@ -969,16 +1045,43 @@ template <bool kQ4, bool kGrouped>
 cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& mb,
                           const CUtensorMap& mdx, const CUtensorMap& mdw, float* y, int64_t M,
                           int64_t N, int64_t K, int64_t ldy, GroupedArgs ga, int n_tiles,
-                          int64_t dense_tiles, cudaStream_t s) {
+                          int64_t dense_tiles, TailArgs ta, cudaStream_t s) {
     cudaError_t e = ensure_smem_attr((const void*)tc_gemm_kernel<kQ4, kGrouped>, SMEM_BYTES,
                                      9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
     if (e != cudaSuccess) return e;
     const bool vec2 = ((uintptr_t)y % 8 == 0) && (ldy % 2 == 0);
     tc_gemm_kernel<kQ4, kGrouped><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
                                                                     ldy, vec2, ga, n_tiles,
-                                                                    dense_tiles);
+                                                                    dense_tiles, ta);
     return cudaGetLastError();
 }
+
+// Tail split of a dense product with `tiles` output tiles and G groups: the
+// tiles of the last, partly empty round of a one-CTA-per-SM grid (all of them
+// when there are fewer tiles than SMs) are cut into the most K chunks that
+// still fit that round, each a multiple of 8 groups.
+struct TailPlan {
+    int64_t full, tail;    // whole-tile units; tail tiles
+    int split;             // chunks per tail tile (1: none)
+};
+
+TailPlan tail_plan(int64_t tiles, int64_t G) {
+    const int64_t sms = sm_count();
+    TailPlan p{tiles, 0, 1};
+    if (sms <= 0) return p;
+    const int64_t L = tiles % sms;
+    if (L == 0) return p;
+    int64_t s = sms / L;
+    while (s > 1 && (G / 8) % s != 0) --s;
+    if (s > 1) {
+        p.full = tiles - L;
+        p.tail = L;
+        p.split = (int)s;
+    }
+    return p;
+}
+
+size_t tail_bytes(const TailPlan& p) { return (size_t)p.tail * p.split * BM * BN * 4; }
 
 int widen_grid(int64_t work) {
     int64_t blocks = (work + 255) / 256;
@@ -1001,10 +1104,14 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const vo
 
 int64_t ldt_of(int64_t N) { return (N + 31) / 32 * 32; }
 
-// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32
+int64_t dense_tile_count(int64_t M, int64_t N) { return ((N + BN - 1) / BN) * ((M + BM - 1) / BM); }
+
+// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32 | the tail
+// tiles' K-chunk partials (binary32, BM x BN each; none without a tail split)
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
     const int64_t G = K / kGroup;
-    return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4);
+    return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4) +
+           tail_bytes(tail_plan(dense_tile_count(M, N), G));
 }
 
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
@@ -1023,12 +1130,21 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, ldt, K, q4))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
-    const int64_t tiles = (int64_t)n_tiles * ((M + BM - 1) / BM);
-    const int64_t ctas = tiles < sm_count() ? tiles : sm_count();
+    const int64_t tiles = dense_tile_count(M, N);
+    const TailPlan tp = tail_plan(tiles, G);
+    const int64_t units = tp.full + tp.tail * tp.split;
+    const int64_t ctas = units < sm_count() ? units : sm_count();
     dim3 grid((unsigned)ctas);
     GroupedArgs ga{};
-    return q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s)
-              : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, tiles, s);
+    float* part = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2) + align16((size_t)G * ldt * 4));
+    const TailArgs ta{(int)tp.full, tp.split, part};
+    e = q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, units, ta, s)
+           : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, units, ta, s);
+    if (e != cudaSuccess || tp.tail == 0) return e;
+    const int64_t elems = tp.tail * BM * BN;
+    tail_reduce_kernel<<<widen_grid(elems), 256, 0, s>>>(part, (int)tp.full, tp.split, (int)tp.tail,
+                                                         n_tiles, M, N, y, ldy);
+    return cudaGetLastError();
 }
 
 // MoE workspace after the routing tables: a16 [P][K] binary16 and dxg [P][G]
@@ -1063,7 +1179,8 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     const int n_tiles = (int)((N + BN - 1) / BN);
     GroupedArgs ga{perm, offsets, tile_offsets, info, E, N};
     dim3 grid((unsigned)sm_count());
-    return launch_kernel<true, true>(grid, ma, mb, mdx, mdw, y, P, N, K, N, ga, n_tiles, 0, s);
+    return launch_kernel<true, true>(grid, ma, mb, mdx, mdw, y, P, N, K, N, ga, n_tiles, 0,
+                                     TailArgs{0, 1, nullptr}, s);
 }
 
 unsigned int read_and_clear_tc_error() {

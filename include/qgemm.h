@@ -75,7 +75,10 @@ const char* qg_status_string(qg_status s);
  * GEMMs pass M, N, K (T, topk, E ignored): M > 8 with K % 256 == 0 runs on the
  * tensor cores and needs M*K*2 bytes (activation codes widened to binary16)
  * plus (K/32)*ceil32(N)*4 bytes (weight scales transposed to binary32), each
- * part padded to 16 bytes; QG_ALGO_TCGEN05 chosen explicitly needs the same
+ * part padded to 16 bytes, plus up to 64 KiB per SM of the current device for
+ * the K-chunk partial sums of the output tiles that would leave the last round
+ * of the one-CTA-per-SM grid partly empty (0 when the 128 x 128 tile count is a
+ * multiple of the SM count); QG_ALGO_TCGEN05 chosen explicitly needs the same
  * for any M (take the size for M = 9 as the floor).  For the MoE GEMM pass K and N and the routing sizes T, topk, E
  * (M ignored).  Workspace pointers must be 16-byte aligned. */
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K,

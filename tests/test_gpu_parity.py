@@ -202,6 +202,25 @@ def test_qgemm_parity(algo, M, N, K, bits):
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_qgemm_tc_whole_tiles_and_split_tail(bits):
+    """More 128 x 128 tiles than SMs, a few left over: whole-tile rounds, then the
+    leftover tiles (ragged rows and columns) cut along K into chunks whose partial
+    sums are added afterwards.  y within tolerance; the same bits on a second run."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_tiles = sms // 2 + 4
+    M, N, K = 200, 128 * n_tiles - 37, 768
+    assert (2 * n_tiles) % sms not in (0, 2 * n_tiles)
+    qx, dx, qw, dw = _case(M, N, K, bits, 4242 + bits)
+    y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
+    args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    y = _gemm(bits, qg.ALGO_TCGEN05, *args)
+    _sync()
+    assert_close(to_np(y), y_ref, mag)
+    assert torch.equal(y, _gemm(bits, qg.ALGO_TCGEN05, *args))
+    assert qg.device_error() == 0
+
+
 @pytest.mark.parametrize("pad", [12, 13])            # even / odd ldy (vector / scalar stores)
 @pytest.mark.parametrize("algo", DENSE_ALGOS)
 def test_qgemm_ldy_and_determinism(algo, pad):
@@ -489,8 +508,14 @@ def test_grouped_moe_unrouted_rows_zero_and_counted(K):
     assert_close(to_np(y), y_ref, mag)
 
 
-@pytest.mark.parametrize("K,algo", [(128, qg.ALGO_MMA), (512, qg.ALGO_TCGEN05)])
+@pytest.mark.parametrize("K,algo", [(128, qg.ALGO_MMA), (256, qg.ALGO_TCGEN05),
+                                     (512, qg.ALGO_TCGEN05)])
 def test_grouped_moe_single_expert_equals_dense_q4(K, algo):
+    """Every row routed to one expert: the MoE product is the dense product of that
+    expert's weights.  Bit for bit where both add the groups in the same order (the
+    MMA kernels; the tensor-core kernels at 8 groups, which the dense kernel never
+    cuts along K).  At 16 groups the dense kernel's 3 tiles, fewer than the SMs, are
+    each summed as two K chunks, so both products are held to the oracle instead."""
     rng, qw4, dw, _ = _moe_small(K=K)
     T = 300
     ids = np.full((T, 1), 6, np.int32)
@@ -499,7 +524,12 @@ def test_grouped_moe_single_expert_equals_dense_q4(K, algo):
     y, _ = qg.grouped_qgemm_moe(qx, dx, to_dev(ids), 0, to_dev(qw4), to_dev(dw))
     yd = qg.qgemm_q4_0(qx, dx, to_dev(qw4[6]), to_dev(dw[6]), algo=algo)
     _sync()
-    assert torch.equal(y, yd)
+    if K == 512:
+        y_ref, mag = oracle.qgemm(to_np(qx), to_np(dx), qw4[6], dw[6], 4)
+        assert_close(to_np(y), y_ref, mag)
+        assert_close(to_np(yd), y_ref, mag)
+    else:
+        assert torch.equal(y, yd)
 
 
 @pytest.fixture(scope="module")
