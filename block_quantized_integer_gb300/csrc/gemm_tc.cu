@@ -13,18 +13,20 @@
 // 2^14 and each group sum an integer below 2^19, which the tensor core
 // accumulates without loss (the group-dot tests check this bit for bit).
 //
-// Per CTA (persistent, one per SM, 704 threads): 128 x 128 output tiles, K
-// walked one pair of 32-groups at a time.
+// Per CTA (persistent, one per SM; 576 threads dense, 704 MoE): 128 x 128
+// output tiles, K walked one pair of 32-groups at a time.
 //   pre-pass    activation codes widened to binary16 once per call (for the
 //               MoE product also gathered into expert order with their
-//               scales); weight scales transposed to group-major binary32.
+//               scales); dense: the weight codes widened to binary16 too and
+//               the weight scales transposed to group-major binary32.
 //   warp 16     TMA producer: binary16 A stages (one pair of groups, 128-byte
-//               swizzle, the operand layout the MMA reads directly), int8 or
-//               packed 4-bit B stages (4 / 8 groups, 128-byte swizzle), dx / dw
+//               swizzle, the operand layout the MMA reads directly); dense: a
+//               binary16 B stage of the same form on the same barrier; MoE:
+//               packed 4-bit B stages (8 groups, 128-byte swizzle); dx / dw
 //               scale stages every 8 groups.
-//   warps 18-21 converters, one B row per thread: B codes -> binary16 into
-//               the canonical K-major no-swizzle layout (8 x 16-byte core
-//               matrices), a pair of groups per operand slot, 4 slots.
+//   warps 18-21 (MoE only) converters, one B row per thread: 4-bit codes ->
+//               binary16 into the canonical K-major no-swizzle layout (8 x
+//               16-byte core matrices), a pair of groups per operand slot.
 //   warp 17     one thread issues, per pair, four K=16 MMAs (two per group,
 //               the first of each overwrites) into one of two 256-column TMEM
 //               pair slots and one commit.
@@ -62,7 +64,8 @@ constexpr int NSC = 3;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
 constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 4;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704: 80 registers a thread
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704 (MoE): 80 registers a thread
+constexpr int THREADS_DENSE = CONV_WARP0 * 32;             // 576 (dense, no converters): 112
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
@@ -92,8 +95,9 @@ constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
 constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
 constexpr uint32_t kSleepHintNs = 20000;             // a waiter sleeps until the phase flips
 
-// full_a: TMA A stage landed; full_ops: the converters saw full_a and wrote
-// the binary16 B pair, so both operands of the slot are ready; done: the
+// full_a: the TMA A stage landed (dense: with the binary16 B stage, so both
+// operands of the slot are ready); full_ops (MoE): the converters saw full_a
+// and wrote the binary16 B pair, so both operands are ready; done: the
 // MMAs of the pair completed (one commit: operand slot free and the pair's
 // accumulators readable); tempty: the epilogue has read the TMEM pair slot;
 // afull (MoE tiles): the MMAs into a TMEM pair slot completed.
@@ -173,53 +177,37 @@ __device__ __forceinline__ uint32_t u4x2_to_h2(uint32_t nib_bytes, uint32_t sel)
     return r;
 }
 
-// Groups gi, gi + 1 of the int8 / packed 4-bit B stage -> the binary16 B pair
+// Groups gi, gi + 1 of the packed 4-bit B stage -> the binary16 B pair
 // (canonical no-swizzle K-major layout: core matrix (row/8, k8) at
 // (row/8)*512 + k8*128, row%8 at +16 each; the second group F16_B further).
 // Thread ct owns B row ct; all its shared loads go out before any store.
-template <bool kQ4>
-__device__ __forceinline__ void convert_pair(const uint8_t* src, uint8_t* dst, int gi, int ct) {
+__device__ __forceinline__ void convert_pair_q4(const uint8_t* src, uint8_t* dst, int gi, int ct) {
     static_assert(CONV_THREADS == BN, "one converter thread per B row");
     const int row = ct, sw = row & 7;
     const uint8_t* srow = src + row * 128;
     uint8_t* drow = dst + (row >> 3) * 512 + sw * 16;
-    if constexpr (!kQ4) {
-        uint4 v[4];                                    // chunks 2 gi .. 2 gi + 3 (16 codes each)
+    uint4 v[2];                                        // one 16-byte group each
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            v[c] = *reinterpret_cast<const uint4*>(srow + (((2 * gi + c) ^ sw) << 4));
+    for (int c = 0; c < 2; ++c)
+        v[c] = *reinterpret_cast<const uint4*>(srow + (((gi + c) ^ sw) << 4));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint4 lo, hi;
-            s8x16_to_h16(v[c], lo, hi);
-            uint8_t* o = drow + (c >> 1) * F16_B + (c & 1) * 256;
-            *reinterpret_cast<uint4*>(o) = lo;
-            *reinterpret_cast<uint4*>(o + 128) = hi;
+    for (int c = 0; c < 2; ++c) {
+        // byte j: element j (low nibble), element j+16 (high nibble)
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        uint32_t lo_h[8], hi_h[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+            lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+            lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+            hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+            hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
         }
-    } else {
-        uint4 v[2];                                    // one 16-byte group each
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-            v[c] = *reinterpret_cast<const uint4*>(srow + (((gi + c) ^ sw) << 4));
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            // byte j: element j (low nibble), element j+16 (high nibble)
-            const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-            uint32_t lo_h[8], hi_h[8];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
-                lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
-                lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
-                hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
-                hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
-            }
-            uint8_t* o = drow + c * F16_B;
-            *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
-            *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
-            *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
-            *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
-        }
+        uint8_t* o = drow + c * F16_B;
+        *reinterpret_cast<uint4*>(o) = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+        *reinterpret_cast<uint4*>(o + 128) = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+        *reinterpret_cast<uint4*>(o + 256) = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+        *reinterpret_cast<uint4*>(o + 384) = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
     }
 }
 
@@ -430,7 +418,7 @@ __device__ __forceinline__ bool epilogue_tile(const Bars& B, const uint8_t* smem
 // Persistent: CTA b takes tiles b, b + gridDim.x, ...  All roles walk the same
 // tile sequence; ring positions and barrier phases run on across tiles.
 template <bool kQ4, bool kGrouped>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(kGrouped ? THREADS : THREADS_DENSE, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_dx, const __grid_constant__ CUtensorMap map_dw,
                float* __restrict__ y, int64_t M, int64_t N, int64_t K, int64_t ldy, bool vec2,
@@ -515,7 +503,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                                         B.full_sc + 8 * slot);
                         ++isc;
                     }
-                    if (g % GB == 0) {
+                    if (kGrouped && g % GB == 0) {
                         const int slot = (int)(ib % NB);
                         if (!(ok = wait_bar<false>(B.empty_b + 8 * slot, ((ib / NB) & 1) ^ 1, abort))) break;
                         mbar_expect_tx(B.full_b + 8 * slot, B_STAGE);
@@ -526,9 +514,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     if (g % GA == 0) {
                         const int slot = (int)(ia % NO);
                         if (!(ok = wait_bar<false>(B.done + 8 * slot, ((ia / NO) & 1) ^ 1, abort))) break;
-                        mbar_expect_tx(B.full_a + 8 * slot, A_STAGE);
+                        mbar_expect_tx(B.full_a + 8 * slot, kGrouped ? A_STAGE : A_STAGE + F16_PAIR);
                         tma_load_2d(sbase + OFF_A + slot * A_STAGE, &map_a, g * 32, (int32_t)T.m0,
                                     B.full_a + 8 * slot);
+                        if constexpr (!kGrouped)       // binary16 weights [N][K]: the pair's 64 columns
+                            tma_load_2d(sbase + OFF_F16 + slot * F16_PAIR, &map_b, g * 32,
+                                        (int32_t)T.bn0, B.full_a + 8 * slot);
                         ++ia;
                     }
                 }
@@ -609,10 +600,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         const int so = (int)(p % NO), ps = (int)(p % NP);
                         const uint32_t po = (uint32_t)((p / NO) & 1), pp = (uint32_t)((p / NP) & 1);
                         // both probes go out back to back; one branch on the pair
-                        const bool ready = mbar_try_wait(B.full_ops + 8 * so, po) &
+                        const bool ready = mbar_try_wait(B.full_a + 8 * so, po) &
                                            mbar_try_wait(B.tempty + 8 * ps, pp ^ 1);
                         if (!ready) {
-                            if (!(ok = wait_bar<false>(B.full_ops + 8 * so, po, abort))) break;
+                            if (!(ok = wait_bar<false>(B.full_a + 8 * so, po, abort))) break;
                             if (!(ok = wait_bar<false>(B.tempty + 8 * ps, pp ^ 1, abort))) break;
                         }
                         tc_fence_after();
@@ -624,7 +615,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const uint64_t da = smem_desc_sw128(a_s + h * 64 + j * 32);
-                                const uint64_t db = smem_desc_noswizzle(b_s + h * F16_B + j * 256, 128, 512);
+                                const uint64_t db = smem_desc_sw128(b_s + h * 64 + j * 32);
                                 mma_f16(d + h * BN, da, db, IDESC, j);
                             }
                         mma_commit(B.done + 8 * so);
@@ -638,13 +629,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             }
         }
     } else if (warp >= CONV_WARP0) {
-        // ------------------------------------------------------------ converters
+      // -------------------------------------------------------------- converters (MoE;
+      // the dense kernel is launched without these warps)
+      if constexpr (kGrouped) {
+        static_assert(kQ4, "the MoE weights are 4-bit");
         const int ct = tid - CONV_WARP0 * 32;
         uint32_t p = 0, sb = 0;                             // run on across tiles
         bool ok = true;
         for (int t = t0; t < num_tiles && ok; t += dt) {
-            const int np = kGrouped ? PAIRS : unit_at(t, PAIRS, ta).pairs;
-            for (int pl = 0; pl < np && ok; ++pl, ++p) {
+            for (int pl = 0; pl < PAIRS && ok; ++pl, ++p) {
                 const int g0 = 2 * pl;
                 if (g0 % GB == 0 && !(ok = wait_bar<true>(B.full_b + 8 * (sb % NB), (sb / NB) & 1, abort))) break;
                 // the operand slot is free once the MMAs of pair p - NO completed
@@ -652,7 +645,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 if (!(ok = wait_bar<true>(B.done + 8 * so, (uint32_t)(((p / NO) & 1) ^ 1), abort))) break;
                 const uint8_t* src = smem + OFF_B + (sb % NB) * B_STAGE;
                 uint8_t* dst = smem + OFF_F16 + so * F16_PAIR;
-                convert_pair<kQ4>(src, dst, g0 % GB, ct);
+                convert_pair_q4(src, dst, g0 % GB, ct);
                 fence_proxy_async_smem();
                 // the A stage of the slot has landed too: full_ops then stands for both
                 if (!(ok = wait_bar<true>(B.full_a + 8 * so, (uint32_t)((p / NO) & 1), abort))) break;
@@ -664,6 +657,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 if ((g0 + 1) % GB == GB - 1) ++sb;
             }
         }
+      }
     } else {
         // ------------------------------------------------------------ epilogue
         if constexpr (kGrouped) {
@@ -845,6 +839,32 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
     }
 }
 
+// Dense Q4 weights -> binary16 [N][K]: one packed 16-byte group per thread
+// step (byte j: element j in the low nibble, element j + 16 in the high
+// nibble, each stored q + 8), written as 64 bytes of binary16 in element order.
+__global__ void __launch_bounds__(256)
+widen_q4_kernel(const uint8_t* __restrict__ qw4, int64_t groups, __half* __restrict__ w16) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < groups;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qw4 + i * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t lo_h[8], hi_h[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t l = w[t] & 0x0f0f0f0fu, h = (w[t] >> 4) & 0x0f0f0f0fu;
+            lo_h[2 * t] = u4x2_to_h2(l, 0x4140);
+            lo_h[2 * t + 1] = u4x2_to_h2(l, 0x4342);
+            hi_h[2 * t] = u4x2_to_h2(h, 0x4140);
+            hi_h[2 * t + 1] = u4x2_to_h2(h, 0x4342);
+        }
+        uint4* o = reinterpret_cast<uint4*>(w16 + i * kGroup);
+        o[0] = make_uint4(lo_h[0], lo_h[1], lo_h[2], lo_h[3]);
+        o[1] = make_uint4(lo_h[4], lo_h[5], lo_h[6], lo_h[7]);
+        o[2] = make_uint4(hi_h[0], hi_h[1], hi_h[2], hi_h[3]);
+        o[3] = make_uint4(hi_h[4], hi_h[5], hi_h[6], hi_h[7]);
+    }
+}
+
 // dwT[r][.] with r = e * G + g: the scale plane transposed to group-major
 // binary32 rows of ldt columns (ldt a multiple of 32), the layout the
 // epilogue reads.  Inside each 32-column block, column 8j + 2c + e is stored
@@ -1019,9 +1039,11 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps of one product: A binary16 [rows][K], B codes [brows][K or K/2],
-// dx [rows][G] (binary32, row-major) and the weight scales: dense, dwT
-// [G][ldt] binary32 (ldt > 0); MoE (ldt == 0), dw [brows][G] binary16 as stored.
+// Tensor maps of one product: A binary16 [rows][K], dx [rows][G] (binary32,
+// row-major), and the weights: dense (ldt > 0), B binary16 [brows][K] (the
+// widened codes, boxes of one pair like A's) and the scales dwT [G][ldt]
+// binary32; MoE (ldt == 0), B codes [brows][K/2] and dw [brows][G] binary16 as
+// stored.
 bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* mdw,
                const void* a16, const void* qw, const float* dx, const void* dws,
                int64_t rows, int64_t brows, int64_t ldt, int64_t K, bool q4) {
@@ -1037,8 +1059,10 @@ bool make_maps(CUtensorMap* ma, CUtensorMap* mb, CUtensorMap* mdx, CUtensorMap* 
                     CU_TENSOR_MAP_SWIZZLE_NONE) &&
            make_map(ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, rows, K * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+           (ldt > 0 ? make_map(mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qw, K, brows, K * 2, 64, BN,
+                               CU_TENSOR_MAP_SWIZZLE_128B)
+                    : make_map(mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, wbytes, brows, wbytes, 128, BN,
+                               CU_TENSOR_MAP_SWIZZLE_128B));
 }
 
 template <bool kQ4, bool kGrouped>
@@ -1050,7 +1074,7 @@ cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& m
                                      9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
     if (e != cudaSuccess) return e;
     const bool vec2 = ((uintptr_t)y % 8 == 0) && (ldy % 2 == 0);
-    tc_gemm_kernel<kQ4, kGrouped><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
+    tc_gemm_kernel<kQ4, kGrouped><<<grid, kGrouped ? THREADS : THREADS_DENSE, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
                                                                     ldy, vec2, ga, n_tiles,
                                                                     dense_tiles, ta);
     return cudaGetLastError();
@@ -1106,12 +1130,13 @@ int64_t ldt_of(int64_t N) { return (N + 31) / 32 * 32; }
 
 int64_t dense_tile_count(int64_t M, int64_t N) { return ((N + BN - 1) / BN) * ((M + BM - 1) / BM); }
 
-// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32 | the tail
-// tiles' K-chunk partials (binary32, BM x BN each; none without a tail split)
+// dense workspace: a16 [M][K] binary16 | dwT [G][ldt(N)] binary32 | w16 [N][K]
+// binary16 (the weight codes widened) | the tail tiles' K-chunk partials
+// (binary32, BM x BN each; none without a tail split)
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
     const int64_t G = K / kGroup;
     return align16((size_t)M * K * 2) + align16((size_t)G * ldt_of(N) * 4) +
-           tail_bytes(tail_plan(dense_tile_count(M, N), G));
+           align16((size_t)N * K * 2) + tail_bytes(tail_plan(dense_tile_count(M, N), G));
 }
 
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
@@ -1120,14 +1145,23 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     const int64_t G = K / kGroup, ldt = ldt_of(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* a16 = reinterpret_cast<__half*>(ws);
-    float* dwt = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2));
+    const size_t off_dwt = align16((size_t)M * K * 2);
+    const size_t off_w16 = off_dwt + align16((size_t)G * ldt * 4);
+    const size_t off_part = off_w16 + align16((size_t)N * K * 2);
+    float* dwt = reinterpret_cast<float*>(ws + off_dwt);
+    __half* w16 = reinterpret_cast<__half*>(ws + off_w16);
     widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
                                                                nullptr, 1, 0);
+    if (q4)
+        widen_q4_kernel<<<widen_grid(N * G), 256, 0, s>>>(static_cast<const uint8_t*>(qw), N * G, w16);
+    else
+        widen_rows_kernel<<<widen_grid(N * (K / 16)), 256, 0, s>>>(
+            static_cast<const int8_t*>(qw), nullptr, N, K, w16, nullptr, nullptr, nullptr, 1, 0);
     transpose_scales_kernel<<<widen_grid(ldt * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
-    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw, dx, dwt, M, N, ldt, K, q4))
+    if (!make_maps(&ma, &mb, &mdx, &mdw, a16, w16, dx, dwt, M, N, ldt, K, q4))
         return cudaErrorInvalidValue;
     const int n_tiles = (int)((N + BN - 1) / BN);
     const int64_t tiles = dense_tile_count(M, N);
@@ -1136,7 +1170,7 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     const int64_t ctas = units < sm_count() ? units : sm_count();
     dim3 grid((unsigned)ctas);
     GroupedArgs ga{};
-    float* part = reinterpret_cast<float*>(ws + align16((size_t)M * K * 2) + align16((size_t)G * ldt * 4));
+    float* part = reinterpret_cast<float*>(ws + off_part);
     const TailArgs ta{(int)tp.full, tp.split, part};
     e = q4 ? launch_kernel<true, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, units, ta, s)
            : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, units, ta, s);

@@ -74,8 +74,9 @@ const char* qg_status_string(qg_status s);
 /* Bytes of device workspace the given call needs (0 if none).  For the dense
  * GEMMs pass M, N, K (T, topk, E ignored): M > 8 with K % 256 == 0 runs on the
  * tensor cores and needs M*K*2 bytes (activation codes widened to binary16)
- * plus (K/32)*ceil32(N)*4 bytes (weight scales transposed to binary32), each
- * part padded to 16 bytes, plus up to 64 KiB per SM of the current device for
+ * plus (K/32)*ceil32(N)*4 bytes (weight scales transposed to binary32) plus
+ * N*K*2 bytes (weight codes widened to binary16), each part padded to 16
+ * bytes, plus up to 64 KiB per SM of the current device for
  * the K-chunk partial sums of the output tiles that would leave the last round
  * of the one-CTA-per-SM grid partly empty (0 when the 128 x 128 tile count is a
  * multiple of the SM count); QG_ALGO_TCGEN05 chosen explicitly needs the same
