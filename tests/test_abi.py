@@ -109,6 +109,21 @@ def test_moe_validation_and_workspace(lib):
     assert g(A, B, 0, 2048, C, 0, 8, 0, D, E, 128, 2048, Y, C, W, ws, S) == 0   # T == 0: no-op
 
 
+def test_dense_tc_workspace_size(lib):
+    """The tensor-core product's workspace as documented: binary16 activation codes, the
+    transposed binary32 weight scales, binary16 weight codes, each padded to 16 bytes, plus
+    whole 64 KiB partial tiles for a tail split (none without a device: 0 SMs)."""
+    def a16(v):
+        return (v + 15) // 16 * 16
+    for op in (1, 2):                                   # Q8_0, Q4_0
+        for M, N, K in ((300, 130, 768), (9, 1, 256), (2048, 12288, 4096), (4000, 33, 512)):
+            G = K // 32
+            base = a16(M * K * 2) + a16(G * ((N + 31) // 32 * 32) * 4) + a16(N * K * 2)
+            ws = lib.qgemm_workspace_size(op, M, N, K, 0, 0, 0)
+            assert ws >= base and (ws - base) % 65536 == 0 and ws - base <= 1024 * 65536
+    assert lib.qgemm_workspace_size(1, 300, 130, 96, 0, 0, 0) == 0     # K % 256 != 0: no TMA path
+
+
 def test_debug_group_dots_validation(lib):
     f = lib.qgemm_debug_group_dots
     ws = lib.qgemm_workspace_size(4, 16, 64, 512, 0, 0, 0)
