@@ -865,23 +865,30 @@ widen_q4_kernel(const uint8_t* __restrict__ qw4, int64_t groups, __half* __restr
     }
 }
 
-// dwT[r][.] with r = e * G + g: the scale plane transposed to group-major
-// binary32 rows of ldt columns (ldt a multiple of 32), the layout the
-// epilogue reads.  Inside each 32-column block, column 8j + 2c + e is stored
-// at 8c + 2j + e (j, c < 4, e < 2), so the 8 columns one epilogue thread
-// scales are contiguous; columns past N are stored as zero.
+// dwT[g][.]: the weight scale plane dw [N][G] (binary16) transposed to
+// group-major binary32 rows of ldt columns (ldt a multiple of 32), the layout
+// the epilogue reads.  Inside each 32-column block, column 8j + 2c + e is
+// stored at 8c + 2j + e (j, c < 4, e < 2), so the 8 columns one epilogue
+// thread scales are contiguous; columns past N are stored as zero.  A block
+// takes 32 columns x 32 groups: dw rows are read along g into shared memory,
+// then dwT rows are written along the stored column (both coalesced).
 __global__ void __launch_bounds__(256)
-transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t rows_n, int64_t G, int64_t E,
+transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t N, int64_t G,
                         float* __restrict__ dwt, int64_t ldt) {
-    const int64_t total = E * ldt * G;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        // i walks dwT in storage order: e, g, stored column (coalesced writes)
-        const int64_t sidx = i % ldt, eg = i / ldt;
-        const int64_t g = eg % G, e = eg / G;
-        const int r = (int)(sidx & 31), c = r >> 3, j = (r >> 1) & 3, el = r & 1;
-        const int64_t n = (sidx & ~(int64_t)31) + 8 * j + 2 * c + el;
-        dwt[eg * ldt + sidx] = n < rows_n ? half_bits_to_float(dw[(e * rows_n + n) * G + g]) : 0.f;
+    __shared__ float tile[32][33];                       // [column][group], padded
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t n0 = (int64_t)blockIdx.x * 32, g0 = (int64_t)blockIdx.y * 32;
+    for (int i = ty; i < 32; i += 8) {                   // column n0 + i, group g0 + tx
+        const int64_t n = n0 + i, g = g0 + tx;
+        tile[i][tx] = (n < N && g < G) ? half_bits_to_float(dw[n * G + g]) : 0.f;
+    }
+    __syncthreads();
+    // stored slot tx of the block holds column 8j + 2c + e
+    const int c = tx >> 3, j = (tx >> 1) & 3, e = tx & 1;
+    const int col = 8 * j + 2 * c + e;
+    for (int i = ty; i < 32; i += 8) {                   // group g0 + i, stored column n0 + tx
+        const int64_t g = g0 + i;
+        if (g < G) dwt[g * ldt + n0 + tx] = tile[col][i];
     }
 }
 
@@ -1157,7 +1164,8 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     else
         widen_rows_kernel<<<widen_grid(N * (K / 16)), 256, 0, s>>>(
             static_cast<const int8_t*>(qw), nullptr, N, K, w16, nullptr, nullptr, nullptr, 1, 0);
-    transpose_scales_kernel<<<widen_grid(ldt * G), 256, 0, s>>>(dw, N, G, 1, dwt, ldt);
+    transpose_scales_kernel<<<dim3((unsigned)(ldt / 32), (unsigned)((G + 31) / 32)), 256, 0, s>>>(
+        dw, N, G, dwt, ldt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
