@@ -59,6 +59,29 @@ def load_peaks():
             "source": "fallback"}
 
 
+def host_cpu():
+    """(logical cores, CPU model) of the host the oracle runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    return os.cpu_count() or 1, model or platform.machine()
+
+
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -111,6 +134,47 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sampled(index, fn):
+    """Run fn() under a clock sampler; returns (fn's result, clock record)."""
+    smp = ClockSampler(index)
+    smp.start()
+    time.sleep(0.2)
+    try:
+        out = fn()
+    finally:
+        clk = smp.stop()
+    return out, clk
+
+
+def event_median_ms(fn, flush, min_reps, min_s=1.0):
+    """Median CUDA-event time of fn() with flush() (an L2 scrub) before every
+    call, outside the timed pair.  The calls are queued back to back, with one
+    synchronize at the end, for at least min_reps calls and about min_s seconds,
+    so that the GPU stays under load while its clocks are sampled."""
+    import torch
+    for _ in range(3):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    flush()
+    fn()
+    b.record()
+    torch.cuda.synchronize()
+    per = max(a.elapsed_time(b), 1e-3) * 1e-3
+    reps = max(min_reps, min(int(min_s / per), 20000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for x, y in evs:
+        flush()
+        x.record()
+        fn()
+        y.record()
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in evs), reps
 
 
 # --------------------------------------------------------------------------- oracle arm
@@ -313,21 +377,14 @@ def prefill_section(dev, peaks, reps=20, long_ctx=False):
         qw, dw = qg.quantize_weight_q8_0(torch.from_numpy(w).to(dev))
         qx, dx = qg.quantize_act_q8(torch.from_numpy(x).to(dev))
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(qg.workspace_size(qg.OP_QGEMM_Q8_0, M, N, K), dtype=torch.uint8,
+                         device=dev)
         scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
-        for _ in range(3):
-            qg.qgemm_q8_0(qx, dx, qw, dw, y=y)
-        ts = []
-        for _ in range(reps):
-            scrub.fill_(1.0)                       # flush L2 (256 MB > 129 MB)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            qg.qgemm_q8_0(qx, dx, qw, dw, y=y)
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ms = statistics.median(ts)
+        # flush L2 (256 MB > 129 MB) before every call
+        ms, n = event_median_ms(lambda: qg.qgemm_q8_0(qx, dx, qw, dw, y=y, workspace=ws),
+                                lambda: scrub.fill_(1.0), reps)
         tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-        out.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops,
+        out.append({"M": M, "N": N, "K": K, "ms": ms, "tops": tops, "reps": n,
                     "frac_of_bf16_peak": tops / peaks["bf16_tflops"]})
         del qw, dw, qx, dx, y, scrub
     return {"unit": "TOPS (int8-equivalent, 2MNK/t)", "shapes": out,
@@ -358,18 +415,9 @@ def moe_section(dev, peaks, reps=20):
         ws = torch.empty(qg.workspace_size(qg.OP_GROUPED_MOE, 0, N, K, ids.shape[0],
                                            ids.shape[1], E), dtype=torch.uint8, device=dev)
         scrub = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
-        for _ in range(3):
-            qg.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw, y=y, d_err=err, workspace=ws)
-        ts = []
-        for _ in range(reps):
-            scrub.fill_(1.0)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            qg.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw, y=y, d_err=err, workspace=ws)
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ms = statistics.median(ts)
+        ms, _ = event_median_ms(
+            lambda: qg.grouped_qgemm_moe(qx, dx, ids, mode, qw4, dw, y=y, d_err=err, workspace=ws),
+            lambda: scrub.fill_(1.0), reps)
         used = np.unique(d["topk_ids"]).size
         nbytes = used * N * K * (0.5 + 2 / 32) + qx.shape[0] * K * (1 + 4 / 32) + P * N * 4
         ops = 2.0 * P * N * K
@@ -576,6 +624,39 @@ def next_rows_section(dev, peaks, reps=20):
     return out
 
 
+def flatten_sections(line, peaks, clocks):
+    """Copy every configured workload's figure to flat scalar keys, at the top
+    level and in the `prefill` dict (a record that keeps only scalars still
+    holds them), with each timed section's clock record beside it."""
+    flat = {}
+    for key, sec in (("prefill", "prefill"), ("longctx", "prefill_long_context")):
+        for r in line[sec]["shapes"]:
+            tag = f"{key}_{r['M']}x{r['N']}x{r['K']}"
+            flat[tag + "_tops"] = r["tops"]
+            flat[tag + "_frac"] = r["frac_of_bf16_peak"]
+            flat[tag + "_ms"] = r["ms"]
+    moe = line["moe"]
+    flat["moe_total_ms"] = moe["total"]["ms"]
+    flat["moe_total_frac_of_hbm"] = moe["total"]["frac_of_hbm"]
+    flat["moe_gate_up_ms"] = moe["gate_up"]["ms"]
+    flat["moe_down_ms"] = moe["down"]["ms"]
+    flat["moe_layer_total_ms"] = line["moe_layer"]["total_ms"]
+    flat["moe_layer_frac_of_hbm"] = line["moe_layer"]["frac_of_hbm_weights"]
+    flat["decode_m4_gbs"] = line["decode_m4"]["gbs"]
+    flat["decode_m4_frac"] = line["decode_m4"]["gbs"] / peaks["hbm_gbs"]
+    for k, v in line["next_rows"].items():
+        if isinstance(v, dict):
+            flat[f"next_{k}_frac"] = v["frac_of_hbm"]
+    for sec, clk in clocks.items():
+        flat[f"{sec}_sm_mhz"] = clk.get("sm_mhz")
+        flat[f"{sec}_clock_samples"] = clk.get("samples", 0)
+        flat[f"{sec}_throttle"] = ",".join(clk.get("reasons", [])) or "none"
+        line["clocks"][f"{sec}_sm_mhz"] = clk.get("sm_mhz")
+        line["clocks"][f"{sec}_reasons"] = ",".join(clk.get("reasons", [])) or "none"
+    line.update(flat)
+    line["prefill"].update(flat)
+
+
 # --------------------------------------------------------------------------- main
 
 def main():
@@ -646,8 +727,8 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
                 "config": {"workload": DECODE_WORKLOAD, "parallelism": "replicas"},
                 "cpu_baseline": {"value": v, "unit": "GB/s",
-                                 "cores": min(oracle.num_threads(), 1),
-                                 "kind": "oracle",
+                                 "cores": oracle.num_threads(), "nproc": host_cpu()[0],
+                                 "cpu_model": host_cpu()[1], "kind": "oracle",
                                  "sample": f"first {frac:.4f} of the rows of each projection "
                                            f"(at most 4096 rows), M=1, per step"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -713,34 +794,40 @@ def main():
     torch.cuda.empty_cache()
 
     if not args.no_extra and rank == 0:
-        projs4 = make_decode(dev, 4)
-        g4 = DecodeGraphs(projs4)
-        ms4, _ = timed(g4.step_full, max(args.steps // 2, 10), 5)
-        b4 = decode_bytes(4, shapes)
-        line["decode_m4"] = {"gbs": b4 * max(args.steps // 2, 10) / (ms4 * 1e-3) / 1e9,
-                             "ms_per_step": ms4 / max(args.steps // 2, 10)}
-        del g4, projs4
+        def m4():
+            projs4 = make_decode(dev, 4)
+            g4 = DecodeGraphs(projs4)
+            n4 = max(args.steps // 2, 10)
+            ms4, _ = timed(g4.step_full, n4, 5)
+            del g4, projs4
+            return decode_bytes(4, shapes) * n4 / (ms4 * 1e-3) / 1e9, ms4 / n4
+        (gbs4, ms4), clk4 = sampled(local, m4)
+        line["decode_m4"] = {"gbs": gbs4, "ms_per_step": ms4}
         torch.cuda.empty_cache()
         line["decode_shapes"] = decode_shapes_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
-        line["prefill"] = prefill_section(dev, peaks, reps=args.reps)
+        line["prefill"], clk_pf = sampled(local, lambda: prefill_section(dev, peaks, reps=args.reps))
         torch.cuda.empty_cache()
-        line["prefill_long_context"] = prefill_section(dev, peaks, reps=max(args.reps // 4, 3),
-                                                       long_ctx=True)
+        line["prefill_long_context"], clk_lc = sampled(
+            local, lambda: prefill_section(dev, peaks, reps=max(args.reps // 4, 3), long_ctx=True))
         torch.cuda.empty_cache()
-        line["moe"] = moe_section(dev, peaks, reps=args.reps)
+        line["moe"], clk_moe = sampled(local, lambda: moe_section(dev, peaks, reps=args.reps))
         line["moe_layer"] = moe_layer_section(dev, peaks, reps=args.reps)
         line["next_rows"] = next_rows_section(dev, peaks, reps=args.reps)
         torch.cuda.empty_cache()
+        flatten_sections(line, peaks, {"decode_m4": clk4, "prefill": clk_pf, "longctx": clk_lc,
+                                       "moe": clk_moe})
 
     if rank == 0:
         _, one, frac, _ = oracle_decode(shapes, 1, 15.0, 1)
         one(frac)
         b, t = one(frac)
         import oracle
-        # the oracle parallelises over activation rows only: M = 1 runs on one core
+        nproc, model = host_cpu()
+        # the oracle splits its output rows into column chunks over OpenMP threads
         line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s",
-                                "cores": min(oracle.num_threads(), 1), "kind": "oracle",
+                                "cores": oracle.num_threads(), "nproc": nproc, "cpu_model": model,
+                                "kind": "oracle",
                                 "sample": f"first {frac:.4f} of the rows of each projection "
                                           f"(at most 4096 rows), M=1, one step"}
         print(json.dumps(line), flush=True)

@@ -85,6 +85,8 @@ def quantize_act_q8(x: torch.Tensor, qx: torch.Tensor | None = None,
         dx = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
     _need(qx, torch.int8, "qx", x.device)
     _need(dx, torch.float32, "dx", x.device)
+    if tuple(qx.shape) != (M, K) or tuple(dx.shape) != (M, K // 32):
+        raise ValueError(f"qx must be [{M}, {K}] and dx [{M}, {K // 32}]")
     _native.call("quantize_act_q8", _ptr(x), M, K, x.stride(0), _ptr(qx), _ptr(dx),
                  _stream(x.device))
     return qx, dx
@@ -111,20 +113,28 @@ def quantize_weight_q4_0(w: torch.Tensor):
 
 
 def _dense(name, qx, dx, qw, dw, y, algo, workspace, wdtype, kfac):
+    # shapes first (they need no device), then dtypes and devices
+    for t, nm in ((qx, "qx"), (dx, "dx"), (qw, "qw"), (dw, "dw")):
+        if not isinstance(t, torch.Tensor) or t.dim() != 2:
+            raise ValueError(f"{nm} must be a 2-D tensor")
+    M, K = qx.shape
+    N = qw.shape[0]
+    if qw.shape[1] * kfac != K or dw.shape != (N, K // 32) or dx.shape != (M, K // 32):
+        raise ValueError("shape mismatch between qx/dx/qw/dw")
+    if y is not None:
+        if not isinstance(y, torch.Tensor) or y.dim() != 2 or y.stride(1) != 1:
+            raise ValueError("y must be a 2-D tensor with unit column stride")
+        if y.shape[0] < M or y.shape[1] < N:
+            raise ValueError(f"y must have at least [{M}, {N}] elements, got {tuple(y.shape)}")
     _need(qx, torch.int8, "qx")
     dev = qx.device
     _need(dx, torch.float32, "dx", dev)
     _need(qw, wdtype, "qw", dev)
     _need(dw, torch.float16, "dw", dev)
-    M, K = qx.shape
-    N = qw.shape[0]
-    if qw.shape[1] * kfac != K or dw.shape != (N, K // 32) or dx.shape != (M, K // 32):
-        raise ValueError("shape mismatch between qx/dx/qw/dw")
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    else:
-        if y.dtype != torch.float32 or y.device != dev or y.stride(1) != 1:
-            raise ValueError("y must be float32 on the same device with unit column stride")
+    elif y.dtype != torch.float32 or y.device != dev:
+        raise ValueError("y must be float32 on the same device")
     if workspace is None:
         op = OP_QGEMM_Q8_0 if kfac == 1 else OP_QGEMM_Q4_0
         nbytes = workspace_size(op, M, N, K)
@@ -255,6 +265,8 @@ def moe_swiglu_quant(gu: torch.Tensor, F: int | None = None):
     P = gu.shape[0]
     if F is None:
         F = gu.shape[1] // 2
+    if gu.shape[1] < 2 * F:
+        raise ValueError(f"gu must have at least 2F = {2 * F} columns, got {gu.shape[1]}")
     qh = torch.empty((P, F), dtype=torch.int8, device=gu.device)
     dh = torch.empty((P, F // 32), dtype=torch.float32, device=gu.device)
     _native.call("moe_swiglu_quant", _ptr(gu), P, F, gu.stride(0), _ptr(qh), _ptr(dh),
@@ -276,6 +288,8 @@ def moe_combine(y: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = Non
         out = torch.empty((T, N), dtype=torch.float32, device=dev)
     else:
         _need(out, torch.float32, "out", dev)
+        if tuple(out.shape) != (T, N):
+            raise ValueError(f"out must be [{T}, {N}], got {tuple(out.shape)}")
     _native.call("moe_combine", _ptr(y), _ptr(w), T, topk, N, _ptr(out), _stream(dev))
     return out
 
@@ -313,23 +327,54 @@ def moe_route(topk_ids: torch.Tensor, E: int, d_err: torch.Tensor | None = None)
     return counts, offsets, perm, d_err
 
 
+def _moe_shapes(qx, dx, topk_ids, qw4, dw, y, d_err):
+    """Shape checks of the grouped MoE product, before anything reaches the
+    library: a short y or weight plane would otherwise be written or read past
+    its end by the kernels.  Returns (rows_x, K, T, topk, E, N)."""
+    for t, nm, nd in ((qx, "qx", 2), (dx, "dx", 2), (topk_ids, "topk_ids", 2), (qw4, "qw4", 3),
+                      (dw, "dw", 3)):
+        if not isinstance(t, torch.Tensor) or t.dim() != nd:
+            raise ValueError(f"{nm} must be a {nd}-D tensor")
+    rows_x, K = qx.shape
+    T, topk = topk_ids.shape
+    E, N = qw4.shape[0], qw4.shape[1]
+    if K % 32 != 0:
+        raise ValueError(f"K = {K} is not a multiple of 32")
+    if tuple(dx.shape) != (rows_x, K // 32):
+        raise ValueError(f"dx must be [{rows_x}, {K // 32}], got {tuple(dx.shape)}")
+    if tuple(qw4.shape) != (E, N, K // 2):
+        raise ValueError(f"qw4 must be [E, N, {K // 2}], got {tuple(qw4.shape)}")
+    if tuple(dw.shape) != (E, N, K // 32):
+        raise ValueError(f"dw must be [{E}, {N}, {K // 32}], got {tuple(dw.shape)}")
+    if y is not None and (not isinstance(y, torch.Tensor) or tuple(y.shape) != (T * topk, N)
+                          or not y.is_contiguous()):
+        raise ValueError(f"y must be a contiguous [{T * topk}, {N}] tensor")
+    if d_err is not None and (not isinstance(d_err, torch.Tensor) or d_err.numel() < 1):
+        raise ValueError("d_err must hold at least one int32")
+    return rows_x, K, T, topk, E, N
+
+
 def grouped_qgemm_moe(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y=None, d_err=None,
                       workspace=None):
     """Per routed pair p: y[p] = x_row(p) @ W_{e(p)}^T with Q4_0 expert weights
     qw4 [E, N, K/2], dw float16 [E, N, K/32]; y [T*topk, N] in (token, slot) order."""
+    rows_x, K, T, topk, E, N = _moe_shapes(qx, dx, topk_ids, qw4, dw, y, d_err)
     _need(qx, torch.int8, "qx")
     dev = qx.device
     _need(dx, torch.float32, "dx", dev)
     _need(topk_ids, torch.int32, "topk_ids", dev)
     _need(qw4, torch.uint8, "qw4", dev)
     _need(dw, torch.float16, "dw", dev)
-    rows_x, K = qx.shape
-    T, topk = topk_ids.shape
-    E, N = qw4.shape[0], qw4.shape[1]
     if y is None:
         y = torch.empty((T * topk, N), dtype=torch.float32, device=dev)
+    else:
+        _need(y, torch.float32, "y", dev)
     if d_err is None:
         d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    else:
+        _need(d_err, torch.int32, "d_err", dev)
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace", dev)
     if workspace is None:
         nbytes = workspace_size(OP_GROUPED_MOE, 0, N, K, T, topk, E)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
@@ -344,6 +389,9 @@ def grouped_qgemm_moe_noalloc(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y, d_e
     routing scratch is a fixed array inside the library (at most 65536 routed
     pairs and 1024 experts).  For callers that cannot allocate device memory,
     y and d_err (zeroed by the caller) must be passed in."""
+    if y is None or d_err is None:
+        raise ValueError("y and d_err must be passed in: this entry point allocates nothing")
+    rows_x, K, T, topk, E, N = _moe_shapes(qx, dx, topk_ids, qw4, dw, y, d_err)
     _need(qx, torch.int8, "qx")
     dev = qx.device
     _need(dx, torch.float32, "dx", dev)
@@ -352,9 +400,6 @@ def grouped_qgemm_moe_noalloc(qx, dx, topk_ids, x_row_mode: int, qw4, dw, y, d_e
     _need(dw, torch.float16, "dw", dev)
     _need(y, torch.float32, "y", dev)
     _need(d_err, torch.int32, "d_err", dev)
-    rows_x, K = qx.shape
-    T, topk = topk_ids.shape
-    E, N = qw4.shape[0], qw4.shape[1]
     _native.call("grouped_qgemm_moe_noalloc", _ptr(qx), _ptr(dx), rows_x, K, _ptr(topk_ids), T,
                  topk, int(x_row_mode), _ptr(qw4), _ptr(dw), E, N, _ptr(y), _ptr(d_err),
                  _stream(dev))

@@ -149,7 +149,7 @@ DebugWs debug_ws(int64_t M, int64_t N, int64_t K) {
 size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, int32_t topk,
                             int32_t E) {
     if (op == QG_OP_GROUPED_MOE) {
-        if (T < 0 || topk <= 0 || E <= 0) return 0;
+        if (T < 0 || topk <= 0 || E <= 0 || T > ((1ll << 31) - 1) / topk) return 0;
         size_t w = moe_ws(T * topk, E).total;
         if (moe_use_tc(K) && N > 0) w += qg::tc_grouped_workspace(T * topk, N, K, E);
         return w;
@@ -238,7 +238,7 @@ qg_status qgemm_q4_0_ex(const int8_t* qx, const float* dx, int64_t M, int64_t N,
 qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* d_err,
                     cudaStream_t stream) {
-    if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || T * (int64_t)topk >= (1ll << 31))
+    if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || T > ((1ll << 31) - 1) / topk)
         return QG_ERR_INVALID_ARG;
     if ((T > 0 && !topk_ids) || !counts || !offsets || !perm || !d_err) return QG_ERR_INVALID_ARG;
     if (((uintptr_t)topk_ids | (uintptr_t)counts | (uintptr_t)offsets | (uintptr_t)perm |
@@ -254,7 +254,7 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
                             int32_t E, int64_t N, float* y, int32_t* d_err, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream) {
     if (T < 0 || topk <= 0 || E <= 0 || E > 1024 || N <= 0 || K <= 0 || K % kGroup != 0 ||
-        (x_row_mode != 0 && x_row_mode != 1) || T * (int64_t)topk >= (1ll << 31))
+        (x_row_mode != 0 && x_row_mode != 1) || T > ((1ll << 31) - 1) / topk)
         return QG_ERR_INVALID_ARG;
     const int64_t P = T * topk;
     if (rows_x < (x_row_mode ? P : T)) return QG_ERR_INVALID_ARG;

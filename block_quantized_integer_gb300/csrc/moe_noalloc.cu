@@ -76,7 +76,8 @@ extern "C" qg_status grouped_qgemm_moe_noalloc(const int8_t* qx, const float* dx
     if (T < 0 || topk <= 0 || E <= 0 || N <= 0 || K <= 0 || K % 32 != 0 ||
         (x_row_mode != 0 && x_row_mode != 1))
         return QG_ERR_INVALID_ARG;
-    if (E > kMaxExperts || T * (int64_t)topk > kMaxPairs) return QG_ERR_UNSUPPORTED;
+    // T is bounded before the product is formed, so T * topk cannot overflow
+    if (E > kMaxExperts || T > kMaxPairs / topk) return QG_ERR_UNSUPPORTED;
     const int64_t P = T * topk;
     if (rows_x < (x_row_mode ? P : T)) return QG_ERR_INVALID_ARG;
     if (T == 0) return QG_OK;

@@ -270,8 +270,12 @@ qg_status kv3_decode(const uint32_t* codes, const float* scales, int64_t T, int3
  * iteration in binary64 and rounded to binary32. */
 void qg_kv3_codebook(float* levels, float* thresholds);
 
-/* grouped_qgemm_moe for callers that cannot allocate device memory: same
- * arguments, results and errors as grouped_qgemm_moe, minus the workspace.
+/* grouped_qgemm_moe for callers that cannot allocate device memory: the same
+ * arguments minus the workspace.  The product always runs on the warp-level
+ * MMA kernel (grouped_qgemm_moe takes the tensor-core kernel when K % 256 == 0),
+ * so its y agrees with grouped_qgemm_moe's within the parity tolerance rather
+ * than bit for bit.  Errors are grouped_qgemm_moe's, except that E > 1024 or
+ * T * topk > 65536 return QG_ERR_UNSUPPORTED (the scratch array's limits).
  * (No counterpart in the pages this library follows: it exists for callers
  * such as a serving process whose device memory is reserved up front by its
  * own pool allocator and that may not call cudaMalloc while running, or a

@@ -188,14 +188,16 @@ void orc_group_dots(const int8_t* qx, int64_t M, int64_t N, int64_t K,
 
 /* ---- y = sum_g dw * dx * S --------------------------------------------------- */
 
-/* One output row: y[n] for n in [0, N), from activation row (qxr, dxr) and the
- * weight rows of one matrix. mag[n] = sum_g |dw * dx * S| (binary64), the scale
- * of the terms that the tolerance of a reordered binary32 sum refers to. */
-static void row_product(const int8_t* qxr, const float* dxr, int64_t N, int64_t K,
+/* Columns [n0, n1) of one output row: y[n] from activation row (qxr, dxr) and
+ * the weight rows of one matrix. mag[n] = sum_g |dw * dx * S| (binary64), the
+ * scale of the terms that the tolerance of a reordered binary32 sum refers to.
+ * Every y[n] is computed on its own, so how the columns are split among
+ * threads does not change any result. */
+static void row_product(const int8_t* qxr, const float* dxr, int64_t n0, int64_t n1, int64_t K,
                         const void* qw, int wbits, const uint16_t* dw,
                         float* yr, double* magr) {
     int64_t G = K / ORC_GROUP;
-    for (int64_t n = 0; n < N; ++n) {
+    for (int64_t n = n0; n < n1; ++n) {
         double acc = 0.0, mag = 0.0;
         for (int64_t g = 0; g < G; ++g) {
             int64_t s = 0;
@@ -214,17 +216,25 @@ static void row_product(const int8_t* qxr, const float* dxr, int64_t N, int64_t 
     }
 }
 
+/* Column chunk of the work split: threads take (row, chunk) items, so a
+ * product with one activation row (decode) still uses every core. */
+#define ORC_NCHUNK 64
+
 /* Dense GEMM/GEMV: y [M][ldy] (binary32), mag [M][N] (binary64, may be NULL). */
 void orc_qgemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                const void* qw, int wbits, const uint16_t* dw,
                float* y, int64_t ldy, double* mag) {
     int64_t G = K / ORC_GROUP;
+    int64_t chunks = (N + ORC_NCHUNK - 1) / ORC_NCHUNK;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)
 #endif
-    for (int64_t m = 0; m < M; ++m)
-        row_product(qx + m * K, dx + m * G, N, K, qw, wbits, dw,
+    for (int64_t it = 0; it < M * chunks; ++it) {
+        int64_t m = it / chunks, n0 = (it % chunks) * ORC_NCHUNK;
+        int64_t n1 = n0 + ORC_NCHUNK < N ? n0 + ORC_NCHUNK : N;
+        row_product(qx + m * K, dx + m * G, n0, n1, K, qw, wbits, dw,
                     y + m * ldy, mag ? mag + m * N : NULL);
+    }
 }
 
 /* Same as orc_qgemm for a listed subset of activation rows: row i of y/mag is
@@ -237,7 +247,7 @@ void orc_qgemm_rows(const int8_t* qx, const float* dx, const int64_t* rows, int6
 #pragma omp parallel for schedule(dynamic, 1)
 #endif
     for (int64_t i = 0; i < R; ++i)
-        row_product(qx + rows[i] * K, dx + rows[i] * G, N, K, qw, wbits, dw,
+        row_product(qx + rows[i] * K, dx + rows[i] * G, 0, N, K, qw, wbits, dw,
                     y + i * N, mag ? mag + i * N : NULL);
 }
 
@@ -293,7 +303,7 @@ int64_t orc_grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t K,
             continue;
         }
         int64_t r = x_row_mode ? p : p / topk;
-        row_product(qx + r * K, dx + r * G, N, K,
+        row_product(qx + r * K, dx + r * G, 0, N, K,
                     qw4 + (int64_t)e * N * (K / 2), 4, dw + (int64_t)e * N * G,
                     y + p * N, mag ? mag + p * N : NULL);
     }

@@ -107,6 +107,17 @@ def test_moe_validation_and_workspace(lib):
     assert lib.moe_route(A, 10, 2, 2000, B, C, D, Y, S) == 1
     assert lib.moe_route(NUL, 10, 2, 16, B, C, D, Y, S) == 1     # null ids with T > 0
     assert g(A, B, 0, 2048, C, 0, 8, 0, D, E, 128, 2048, Y, C, W, ws, S) == 0   # T == 0: no-op
+    # T * topk past int64 range: rejected before the product is formed
+    huge = (1 << 62) + 1
+    assert g(A, B, huge, 2048, C, huge, 8, 0, D, E, 128, 2048, Y, C, W, ws, S) == 1
+    assert lib.moe_route(A, huge, 8, 16, B, C, D, Y, S) == 1
+    assert lib.qgemm_workspace_size(3, 0, 2048, 2048, huge, 8, 128) == 0
+    assert lib.grouped_qgemm_moe_noalloc(A, B, huge, 2048, C, huge, 8, 0, D, E, 128, 2048, Y, C,
+                                         S) == 5
+    assert lib.grouped_qgemm_moe_noalloc(A, B, 70000, 2048, C, 70000, 1, 0, D, E, 128, 2048, Y,
+                                         C, S) == 5      # more routed pairs than the array holds
+    assert lib.grouped_qgemm_moe_noalloc(A, B, 947, 2048, C, 947, 8, 0, D, E, 1025, 2048, Y,
+                                         C, S) == 5      # more experts than the array holds
 
 
 def test_dense_tc_workspace_size(lib):

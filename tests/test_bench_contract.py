@@ -26,3 +26,30 @@ def test_reference_arm_json_line():
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert "workload" in d["config"]
+
+
+def test_flatten_sections_keeps_scalars():
+    """Every configured workload's figure lands in flat scalar keys (top level and in
+    the `prefill` dict), with each section's clock record beside it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    shp = lambda M, N, K: {"M": M, "N": N, "K": K, "ms": 1.0, "tops": 500.0,
+                           "frac_of_bf16_peak": 0.25}
+    line = {"clocks": {"sm_mhz": 2070.0},
+            "prefill": {"shapes": [shp(2048, 12288, 4096), shp(2048, 4096, 12288)]},
+            "prefill_long_context": {"shapes": [shp(18432, 17408, 5120), shp(18432, 5120, 17408)]},
+            "moe": {"total": {"ms": 0.6, "frac_of_hbm": 0.14}, "gate_up": {"ms": 0.4},
+                    "down": {"ms": 0.2}},
+            "moe_layer": {"total_ms": 0.65, "frac_of_hbm_weights": 0.1},
+            "decode_m4": {"gbs": 4600.0},
+            "next_rows": {"kv3_encode": {"frac_of_hbm": 0.5}, "l2": "flushed"}}
+    clk = {"sm_mhz": 2070.0, "samples": 12, "reasons": []}
+    bench.flatten_sections(line, {"hbm_gbs": 6680.8},
+                           {"prefill": clk, "longctx": clk, "moe": clk, "decode_m4": clk})
+    for k in ("prefill_2048x12288x4096_tops", "prefill_2048x4096x12288_tops",
+              "longctx_18432x17408x5120_tops", "longctx_18432x5120x17408_tops", "moe_total_ms",
+              "prefill_sm_mhz", "moe_throttle", "decode_m4_frac", "next_kv3_encode_frac"):
+        assert k in line and k in line["prefill"], k
+        assert not isinstance(line[k], (list, dict))
+    assert line["clocks"]["prefill_reasons"] == "none"
+    json.dumps(line)

@@ -660,12 +660,23 @@ def test_moe_layer_end_to_end():
     yd, _ = qg.grouped_qgemm_moe(qh, dh, to_dev(ids), 1, to_dev(qdn), to_dev(ddn))
     out = qg.moe_combine(yd, to_dev(w))
     _sync()
-    flips = int((to_np(qh) != qh_ref).sum())
-    assert flips <= qh_ref.size // 1000            # codes differ only at near-ties
-    # a flipped code moves one down-projection term by one quantum of its row
+    qh_np = to_np(qh)
+    flip = qh_np != qh_ref
+    assert int(flip.sum()) <= qh_ref.size // 1000    # codes differ only at near-ties
+    assert np.all(np.abs(qh_np.astype(np.int32) - qh_ref.astype(np.int32))[flip] == 1)
+    # A code flipped by one in pair row p, group g moves y_down[p, n] by at most
+    # dh[p, g] * dw[e(p), n, g] * max|q4| (|q4| <= 8); only the tokens holding
+    # such a pair get that extra allowance, every other token keeps the 1e-5 bar.
+    dwn = oracle.f16_bits_to_f32(ddn).astype(np.float64).reshape(ddn.shape)   # [E, K, F/32]
+    dh_hi = np.maximum(to_np(dh), dh_ref).astype(np.float64)   # either side's group scale
+    extra = np.zeros((T * topk, K))
+    for p, k in zip(*np.nonzero(flip)):
+        g = k // 32
+        extra[p] += dh_hi[p, g] * dwn[ids.reshape(-1)[p], :, g] * 8.0
     wsum = np.abs(w[:, :, None].astype(np.float64) * yd_mag.reshape(T, topk, K)).sum(1)
+    wextra = (w[:, :, None].astype(np.float64) * extra.reshape(T, topk, K)).sum(1)
     err = np.abs(to_np(out).astype(np.float64) - out_ref)
-    assert np.all(err <= 1e-5 * wsum + 1e-4 * wsum * (flips > 0) + 1e-30)
+    assert np.all(err <= 1e-5 * wsum + wextra + 1e-30)
 
 
 # ------------------------------------------------------------------ GGUF block import
