@@ -96,7 +96,7 @@ qg_status dense(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t
             return from_cuda(qg::launch_mma_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, s));
         case QG_ALGO_TCGEN05:
             if (!qg::tc_gemm_supported(M, N, K, dx, dw)) return QG_ERR_UNSUPPORTED;
-            if (!ws || ws_bytes < qg::tc_gemm_workspace(M, N, K) || !aligned16(ws))
+            if (!ws || ws_bytes < qg::tc_gemm_workspace(M, N, K, q4) || !aligned16(ws))
                 return QG_ERR_WORKSPACE;
             return from_cuda(qg::launch_tc_gemm(qx, dx, M, N, K, qw, q4, dw, y, ldy, ws, s));
         default:
@@ -125,8 +125,11 @@ int qg_device_sm_count(void) { return qg::sm_count(); }
 unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 
 // The grouped product runs on the tensor cores when K % 256 == 0 (TMA scale
-// boxes), else on the warp-MMA kernel.
-bool moe_use_tc(int64_t K) { return K > 0 && K % 256 == 0; }
+// boxes) and the expert weight planes (E * N rows) stay within 32-bit TMA
+// coordinates, else on the warp-MMA kernel.
+bool moe_use_tc(int64_t K, int32_t E, int64_t N) {
+    return K > 0 && K % 256 == 0 && (int64_t)E * N < (1ll << 31) - 256;
+}
 
 // Debug group-dot workspace: dx = 1 [M][G] f32 | dw one-hot [N][G] binary16 |
 // y [M][N] f32 | the dense product's workspace (sized for any algo).
@@ -141,7 +144,7 @@ DebugWs debug_ws(int64_t M, int64_t N, int64_t K) {
     w.dw = o;   o = align_up(o + 2 * (size_t)(N * G), 16);
     w.y = o;    o = align_up(o + 4 * (size_t)(M * N), 16);
     w.prod = o;
-    if (K % 256 == 0) o += qg::tc_gemm_workspace(M > 9 ? M : 9, N, K);
+    if (K % 256 == 0) o += qg::tc_gemm_workspace(M > 9 ? M : 9, N, K, false);   // Q8 needs more than Q4
     w.total = o;
     return w;
 }
@@ -151,7 +154,7 @@ size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, 
     if (op == QG_OP_GROUPED_MOE) {
         if (T < 0 || topk <= 0 || E <= 0 || T > ((1ll << 31) - 1) / topk) return 0;
         size_t w = moe_ws(T * topk, E).total;
-        if (moe_use_tc(K) && N > 0) w += qg::tc_grouped_workspace(T * topk, N, K, E);
+        if (moe_use_tc(K, E, N) && N > 0) w += qg::tc_grouped_workspace(T * topk, N, K, E);
         return w;
     }
     if (op == QG_OP_DEBUG_GROUP_DOTS) {
@@ -160,7 +163,8 @@ size_t qgemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t T, 
     }
     if (op == QG_OP_QGEMM_Q8_0 || op == QG_OP_QGEMM_Q4_0) {
         // the tensor-core path widens the activation codes to binary16 first
-        if (M > 8 && K > 0 && K % 256 == 0) return qg::tc_gemm_workspace(M, N, K);
+        if (M > 8 && K > 0 && K % 256 == 0)
+            return qg::tc_gemm_workspace(M, N, K, op == QG_OP_QGEMM_Q4_0);
         return 0;
     }
     return 0;
@@ -265,7 +269,7 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
         ((uintptr_t)dw & 1u))
         return QG_ERR_ALIGNMENT;
     const MoeWs w = moe_ws(P, E);
-    const bool tc = moe_use_tc(K) && ((uintptr_t)dx % 16 == 0) && ((uintptr_t)dw % 16 == 0);
+    const bool tc = moe_use_tc(K, E, N) && ((uintptr_t)dx % 16 == 0) && ((uintptr_t)dw % 16 == 0);
     const size_t need = w.total + (tc ? qg::tc_grouped_workspace(P, N, K, E) : 0);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QG_ERR_WORKSPACE;
     uint8_t* ws = (uint8_t*)workspace;

@@ -43,7 +43,7 @@ cudaError_t launch_mma_grouped(const int8_t* qx, const float* dx, int64_t P, int
                                const GatherArgs& ga, cudaStream_t s);
 
 bool tc_gemm_supported(int64_t M, int64_t N, int64_t K, const void* dx, const void* dw);
-size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K);
+size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K, bool q4);
 cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t N, int64_t K,
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s);
