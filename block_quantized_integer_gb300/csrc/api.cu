@@ -144,7 +144,11 @@ DebugWs debug_ws(int64_t M, int64_t N, int64_t K) {
     w.dw = o;   o = align_up(o + 2 * (size_t)(N * G), 16);
     w.y = o;    o = align_up(o + 4 * (size_t)(M * N), 16);
     w.prod = o;
-    if (K % 256 == 0) o += qg::tc_gemm_workspace(M > 9 ? M : 9, N, K, false);   // Q8 needs more than Q4
+    if (K % 256 == 0) {       // either weight format (their tiles, hence tail splits, differ)
+        const int64_t m = M > 9 ? M : 9;
+        const size_t q8 = qg::tc_gemm_workspace(m, N, K, false), q4 = qg::tc_gemm_workspace(m, N, K, true);
+        o += q8 > q4 ? q8 : q4;
+    }
     w.total = o;
     return w;
 }

@@ -121,20 +121,17 @@ def test_moe_validation_and_workspace(lib):
 
 
 def test_dense_tc_workspace_size(lib):
-    """The tensor-core product's workspace as documented: binary16 activation codes; for
-    Q8_0 also the transposed binary32 weight scales (columns padded to 256) and the binary16
-    weight codes (Q4_0 codes are unpacked in shared memory), each padded to 16 bytes; plus
-    whole 128 KiB partial tiles for a tail split (none without a device: 0 SMs)."""
+    """The tensor-core product's workspace as documented: binary16 activation codes, the
+    transposed binary32 weight scales, binary16 weight codes, each padded to 16 bytes, plus
+    whole 64 KiB partial tiles for a tail split (none without a device: 0 SMs)."""
     def a16(v):
         return (v + 15) // 16 * 16
     for op in (1, 2):                                   # Q8_0, Q4_0
         for M, N, K in ((300, 130, 768), (9, 1, 256), (2048, 12288, 4096), (4000, 33, 512)):
             G = K // 32
-            base = a16(M * K * 2)
-            if op == 1:
-                base += a16(G * ((N + 255) // 256 * 256) * 4) + a16(N * K * 2)
+            base = a16(M * K * 2) + a16(G * ((N + 31) // 32 * 32) * 4) + a16(N * K * 2)
             ws = lib.qgemm_workspace_size(op, M, N, K, 0, 0, 0)
-            assert ws >= base and (ws - base) % 131072 == 0 and ws - base <= 1024 * 131072
+            assert ws >= base and (ws - base) % 65536 == 0 and ws - base <= 1024 * 65536
     assert lib.qgemm_workspace_size(1, 300, 130, 96, 0, 0, 0) == 0     # K % 256 != 0: no TMA path
 
 

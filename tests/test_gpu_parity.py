@@ -204,17 +204,13 @@ def test_qgemm_parity(algo, M, N, K, bits):
 
 @pytest.mark.parametrize("bits", [8, 4])
 def test_qgemm_tc_whole_tiles_and_split_tail(bits):
-    """More output tiles (128 rows for Q8_0, 64 for Q4_0, x 256 columns) than SMs, a few
-    left over: whole-tile rounds, then the leftover tiles (ragged rows and columns) cut
-    along K into 3 chunks whose partial sums are added afterwards.  y within tolerance;
-    the same bits on a second run."""
+    """More 128 x 128 tiles than SMs, a few left over: whole-tile rounds, then the
+    leftover tiles (ragged rows and columns) cut along K into chunks whose partial
+    sums are added afterwards.  y within tolerance; the same bits on a second run."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    M, K = 200, 768                                   # 24 groups: chunks of 8 groups
-    m_tiles = -(-M // (128 if bits == 8 else 64))
-    n_tiles = -(-(sms + 4) // m_tiles)
-    N = 256 * n_tiles - 37
-    tiles = m_tiles * n_tiles
-    assert tiles > sms and tiles % sms != 0 and sms // (tiles % sms) >= 3
+    n_tiles = sms // 2 + 4
+    M, N, K = 200, 128 * n_tiles - 37, 768
+    assert (2 * n_tiles) % sms not in (0, 2 * n_tiles)
     qx, dx, qw, dw = _case(M, N, K, bits, 4242 + bits)
     y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
     args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
@@ -518,7 +514,7 @@ def test_grouped_moe_single_expert_equals_dense_q4(K, algo):
     """Every row routed to one expert: the MoE product is the dense product of that
     expert's weights.  Bit for bit where both add the groups in the same order (the
     MMA kernels; the tensor-core kernels at 8 groups, which the dense kernel never
-    cuts along K).  At 16 groups the dense kernel's 5 tiles, fewer than the SMs, are
+    cuts along K).  At 16 groups the dense kernel's 3 tiles, fewer than the SMs, are
     each summed as two K chunks, so both products are held to the oracle instead."""
     rng, qw4, dw, _ = _moe_small(K=K)
     T = 300
