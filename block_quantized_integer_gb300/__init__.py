@@ -30,7 +30,7 @@ __all__ = [
     "attn_splitk_merge", "kv3_encode", "kv3_decode", "kv3_codebook",
     "moe_swiglu_quant", "moe_combine",
     "workspace_size", "debug_group_dots",
-    "sm_count", "device_error",
+    "sm_count", "device_error", "debug_set_wait_limit",
 ]
 
 ALGO_AUTO, ALGO_GEMV, ALGO_MMA, ALGO_TCGEN05 = 0, 1, 2, 3
@@ -68,6 +68,12 @@ def sm_count() -> int:
 def device_error() -> int:
     """Read and clear the tensor-core kernels' device error word (0 = none)."""
     return int(_native.load().qg_device_error())
+
+
+def debug_set_wait_limit(cycles: int) -> None:
+    """Test-only: SM cycles a tensor-core pipeline wait may last before the kernel
+    gives up and sets the device error word (cycles <= 0: the default, ~2 s)."""
+    _native.call("qg_debug_set_wait_limit", int(cycles))
 
 
 def workspace_size(op: int, M=0, N=0, K=0, T=0, topk=0, E=0) -> int:

@@ -24,6 +24,7 @@ SIGNATURES = {
     "qg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "qg_device_sm_count": (ctypes.c_int, []),
     "qg_device_error": (ctypes.c_uint, []),
+    "qg_debug_set_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
     "qgemm_workspace_size": (SZ, [ctypes.c_int, I64, I64, I64, I64, I32, I32]),
     "quantize_act_q8": (ctypes.c_int, [P, I64, I64, I64, P, P, P]),
     "quantize_weight_q8_0": (ctypes.c_int, [P, I64, I64, P, P, P]),

@@ -124,6 +124,8 @@ int qg_device_sm_count(void) { return qg::sm_count(); }
 
 unsigned int qg_device_error(void) { return qg::read_and_clear_tc_error(); }
 
+qg_status qg_debug_set_wait_limit(long long cycles) { return from_cuda(qg::set_wait_limit(cycles)); }
+
 // The grouped product runs on the tensor cores when K % 256 == 0 (TMA scale
 // boxes) and the expert weight planes (E * N rows) stay within 32-bit TMA
 // coordinates, else on the warp-MMA kernel.

@@ -48,6 +48,10 @@
 namespace qg {
 
 __device__ unsigned int g_tc_error = 0;
+// Cycles a pipeline wait may last before the kernel gives up (~2 s at 2 GHz);
+// lowered only by the test-only qg_debug_set_wait_limit.
+constexpr long long kWaitCycles = 4000000000ll;
+__device__ long long g_wait_limit = kWaitCycles;
 
 namespace {
 
@@ -92,7 +96,6 @@ static_assert(OFF_B % 1024 == 0 && OFF_F16 % 1024 == 0, "swizzled stages need 1 
 constexpr uint32_t TMEM_COLS = NP * 2 * BN;          // 512: two pair slots of two groups
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr uint32_t kSpinLimit = 1u << 22;          // drain polls after an abort
-constexpr long long kWaitCycles = 4000000000ll;      // ~2 s at 2 GHz: a wait that long has failed
 constexpr uint32_t kSleepHintNs = 20000;             // a waiter sleeps until the phase flips
 
 // full_a: the TMA A stage landed (dense: with the binary16 B stage, so both
@@ -121,7 +124,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t base) {
 }
 
 // Bounded wait: the thread sleeps in try_wait until the phase completes; after
-// kWaitCycles without completion (or when another role gave up) it returns
+// g_wait_limit cycles without completion (or when another role gave up) it returns
 // false.  kWarp: all 32 lanes call it and leave together.
 template <bool kWarp>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -136,7 +139,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
         bool ab = *abort != 0;
         if (kWarp) ab = __any_sync(0xffffffffu, ab);
         if (ab) return false;
-        bool late = clock64() - start > kWaitCycles;
+        bool late = clock64() - start > g_wait_limit;
         if (kWarp) late = __any_sync(0xffffffffu, late);
         if (late) {
             *abort = 1;
@@ -1226,6 +1229,11 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     dim3 grid((unsigned)sm_count());
     return launch_kernel<true, true>(grid, ma, mb, mdx, mdw, y, P, N, K, N, ga, n_tiles, 0,
                                      TailArgs{0, 1, nullptr}, s);
+}
+
+cudaError_t set_wait_limit(long long cycles) {
+    const long long v = cycles > 0 ? cycles : kWaitCycles;
+    return cudaMemcpyToSymbol(g_wait_limit, &v, sizeof v);
 }
 
 unsigned int read_and_clear_tc_error() {

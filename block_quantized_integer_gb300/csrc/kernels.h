@@ -48,6 +48,8 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
                            const void* qw, bool q4, const uint16_t* dw, float* y, int64_t ldy,
                            void* workspace, cudaStream_t s);
 unsigned int read_and_clear_tc_error();
+// Test-only: cycles a tensor-core pipeline wait may last (<= 0: the default).
+cudaError_t set_wait_limit(long long cycles);
 int tc_tile_m();
 size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E);
 cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N, int64_t K,

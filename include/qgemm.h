@@ -299,6 +299,15 @@ qg_status grouped_qgemm_moe_noalloc(const int8_t* qx, const float* dx, int64_t r
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int qg_device_sm_count(void);
 
+/* Test-only (no counterpart in the pages): the number of SM clock cycles a
+ * pipeline wait of the tensor-core kernels may last on the current device
+ * before the kernel gives up (sets bit 0 of the device error word, drains its
+ * own copies and MMAs, frees tensor memory and returns without writing its
+ * tiles).  cycles <= 0 restores the default, about 2 s.  A blocking copy to
+ * the device; it exists so that tests can make a wait run out without
+ * withholding any arrival. */
+qg_status qg_debug_set_wait_limit(long long cycles);
+
 /* Device error word of the tensor-core kernels on the current device, then
  * cleared: 0 = none, bit 0 = a pipeline wait gave up (the kernel abandoned its
  * tile without writing it, after draining its own copies and freeing tensor

@@ -37,6 +37,10 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in _native.SIGNATURES, f"binding lacks {name}"
 
 
+def test_wait_limit_entry_is_test_only_and_declared(lib):
+    assert "qg_debug_set_wait_limit" in _declared()
+
+
 def test_status_strings(lib):
     for code, name in enumerate(["QG_OK", "QG_ERR_INVALID_ARG", "QG_ERR_ALIGNMENT",
                                  "QG_ERR_WORKSPACE", "QG_ERR_CUDA", "QG_ERR_UNSUPPORTED"]):

@@ -221,6 +221,31 @@ def test_qgemm_tc_whole_tiles_and_split_tail(bits):
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_tc_wait_limit_gives_up_and_recovers(bits):
+    """A pipeline wait of the tensor-core kernel that runs out sets the device error
+    word, and the call returns (the kernel drains its own copies and MMAs and frees
+    tensor memory); the next call on the same GPU is correct.  The wait is made to
+    run out by lowering the wait limit to one cycle: nothing is withheld, no trap."""
+    M, N, K = 512, 768, 1024
+    qx, dx, qw, dw = _case(M, N, K, bits, 777 + bits)
+    args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    assert qg.device_error() == 0
+    try:
+        qg.debug_set_wait_limit(1)
+        for _ in range(3):
+            _gemm(bits, qg.ALGO_TCGEN05, *args)
+        _sync()
+        assert qg.device_error() == 1
+    finally:
+        qg.debug_set_wait_limit(0)
+    y_ref, mag = oracle.qgemm(qx, dx, qw, dw, bits)
+    y = _gemm(bits, qg.ALGO_TCGEN05, *args)
+    _sync()
+    assert qg.device_error() == 0
+    assert_close(to_np(y), y_ref, mag)
+
+
 @pytest.mark.parametrize("pad", [12, 13])            # even / odd ldy (vector / scalar stores)
 @pytest.mark.parametrize("algo", DENSE_ALGOS)
 def test_qgemm_ldy_and_determinism(algo, pad):
