@@ -7,7 +7,12 @@
 //                 then h re-quantized to int8 codes + binary32 scale per
 //                 32-group with the activation rule (d = max|h| / 127 by one
 //                 IEEE division, q = clamp(round_half_even(h / d), -127, 127)),
-//                 ready to be the activation rows of the down projection;
+//                 ready to be the activation rows of the down projection.
+//                 Both quotients are taken as a product with a correctly
+//                 rounded binary32 reciprocal (silu: v * rcp(1 + e^-v); codes:
+//                 h * rcp(d)): each differs from the IEEE quotient by at most
+//                 one rounding, so a code can differ from round_half_even(h / d)
+//                 only where h / d lies within ~2^-22 relative of a half-integer;
 //   combine:      out[t, n] = sum_{s < topk} w[t, s] * y[t * topk + s, n], the
 //                 slots summed in order with binary32 FMAs.
 //
@@ -22,12 +27,12 @@ namespace qg {
 namespace {
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
 }
 
-__device__ __forceinline__ int quant127(float v, float d) {
-    if (d == 0.0f) return 0;
-    const int q = __float2int_rn(__fdiv_rn(v, d));
+// rd = rcp(d) (0 when d == 0: every code of an all-zero group is 0)
+__device__ __forceinline__ int quant127(float v, float rd) {
+    const int q = __float2int_rn(__fmul_rn(v, rd));
     return min(max(q, -127), 127);
 }
 
@@ -86,11 +91,12 @@ swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t 
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             const float d = __fdiv_rn(m, 127.0f);
+            const float rd = d == 0.0f ? 0.0f : __frcp_rn(d);
             if (active) {
-                const uint32_t packed = (uint32_t)(quant127(h[0], d) & 0xff) |
-                                        ((uint32_t)(quant127(h[1], d) & 0xff) << 8) |
-                                        ((uint32_t)(quant127(h[2], d) & 0xff) << 16) |
-                                        ((uint32_t)(quant127(h[3], d) & 0xff) << 24);
+                const uint32_t packed = (uint32_t)(quant127(h[0], rd) & 0xff) |
+                                        ((uint32_t)(quant127(h[1], rd) & 0xff) << 8) |
+                                        ((uint32_t)(quant127(h[2], rd) & 0xff) << 16) |
+                                        ((uint32_t)(quant127(h[3], rd) & 0xff) << 24);
                 // [P][F] codes and [P][G] scales at the flat group index
                 *reinterpret_cast<uint32_t*>(qh + grp[u] * kGroup + sub * 4) = packed;
                 if (sub == 0) dh[grp[u]] = d;

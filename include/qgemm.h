@@ -210,8 +210,9 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
  * W4A8 grouped GEMM; the pages do not spell the activation out, the usual
  * gated one is taken):
  *   h[p, j] = silu(gu[p, j]) * gu[p, F + j],  silu(v) = v / (1 + exp(-v)),
- * evaluated in binary32 (expf, IEEE division and products), then per row p
- * and 32-group the activation rule of quantize_act_q8.
+ * evaluated in binary32 (expf, a correctly rounded reciprocal and products),
+ * then per row p and 32-group the activation rule of quantize_act_q8, the
+ * quotient h / d taken as h times the correctly rounded reciprocal of d.
  *   gu: float32 [P][ldgu], ldgu >= 2F, gate in columns [0, F), up in [F, 2F)
  *       (the fused gate/up output of grouped_qgemm_moe);
  *   qh: int8 [P][F] (16-byte aligned), dh: float32 [P][F/32].  F % 32 == 0.
