@@ -13,18 +13,20 @@
 // 2^14 and each group sum an integer below 2^19, which the tensor core
 // accumulates without loss (the group-dot tests check this bit for bit).
 //
-// Per CTA (persistent, one per SM; 576 threads dense, 704 MoE): 128 x 128
+// Per CTA (persistent, one per SM; 576 threads dense, 768 MoE): 128 x 128
 // output tiles, K walked one pair of 32-groups at a time.
 //   pre-pass    activation codes widened to binary16 once per call (for the
 //               MoE product also gathered into expert order with their
 //               scales); dense: the weight codes widened to binary16 too and
 //               the weight scales transposed to group-major binary32.
 //   warp 16     TMA producer: binary16 A stages (one pair of groups, 128-byte
-//               swizzle, the operand layout the MMA reads directly); dense: a
-//               binary16 B stage of the same form on the same barrier; MoE:
-//               packed 4-bit B stages (8 groups, 128-byte swizzle); dx / dw
-//               scale stages every 8 groups.
-//   warps 18-21 (MoE only) converters, one B row per thread: 4-bit codes ->
+//               swizzle, the operand layout the MMA reads directly); dense:
+//               a binary16 B stage of the same form on the same barrier, and
+//               the dx / dw scale stages every 8 groups.
+//   warps 18-19 (MoE only) TMA producers of the packed 4-bit B stages (8
+//               groups, 128-byte swizzle) and of the scale stages, each on its
+//               own thread so that no stream waits behind another's ring.
+//   warps 20-23 (MoE only) converters, one B row per thread: 4-bit codes ->
 //               binary16 into the canonical K-major no-swizzle layout (8 x
 //               16-byte core matrices), a pair of groups per operand slot.
 //   warp 17     one thread issues, per pair, four K=16 MMAs (two per group,
@@ -64,12 +66,15 @@ constexpr int NB = 4;                  // B code stages (each 128-byte rows: 4 Q
 constexpr int NP = 2;                  // TMEM pair slots (two 128-column accumulators each)
 constexpr int NPMAX = 8;               // MoE pair slots at most (narrow tiles: 8 x 2 x 32 columns)
 constexpr int SCG = 8;                 // groups per scale stage
-constexpr int NSC = 3;                 // scale stages
+constexpr int NSC = 4;                 // scale stages
 constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter, 32 columns each
-constexpr int PROD_WARP = 16, MMA_WARP = 17, CONV_WARP0 = 18, CONV_WARPS = 4;
+constexpr int PROD_WARP = 16, MMA_WARP = 17, BPROD_WARP = 18, SPROD_WARP = 19;
+constexpr int CONV_WARP0 = 20, CONV_WARPS = 4;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 704 (MoE): 80 registers a thread
-constexpr int THREADS_DENSE = CONV_WARP0 * 32;             // 576 (dense, no converters): 112
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // 768 (MoE): 80 registers a thread
+constexpr int THREADS_DENSE = (MMA_WARP + 1) * 32;         // 576 (dense: warps 0-17 only): 96
+static_assert(MMA_WARP + 1 == 18 && PROD_WARP < MMA_WARP && EPI_WARPS == PROD_WARP,
+              "the dense kernel launches epilogue, producer and MMA warps only");
 
 constexpr int A_STAGE = BM * 128;                    // 16384
 constexpr int B_STAGE = BN * 128;                    // 16384
@@ -476,9 +481,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == PROD_WARP) {
-        // ------------------------------------------------------------ producer
+    const bool producer = warp == PROD_WARP || (kGrouped && (warp == BPROD_WARP || warp == SPROD_WARP));
+    if (producer) {
+        // ------------------------------------------------------------ producers
+        // Dense: one thread issues every stream.  MoE: one thread per stream
+        // (A stages, 4-bit B stages, scale stages), so that no stream waits
+        // behind another's ring: the scale stages are released by the
+        // epilogue, which runs up to a TMEM ring behind the MMAs.
         if (lane == 0) {
+            const bool do_a = warp == PROD_WARP;
+            const bool do_b = kGrouped && warp == BPROD_WARP;
+            const bool do_sc = !kGrouped || warp == SPROD_WARP;
             int64_t ia = 0, ib = 0, isc = 0;      // stages issued so far (run on across tiles)
             bool ok = true;
             for (int t = t0; t < num_tiles && ok; t += dt) {
@@ -492,7 +505,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 const Tile T = tile_at<kGrouped>(tile, M, G, ga, n_tiles);
                 // issue in the order the stages are first needed
                 for (int g = gb; g < ge && ok; ++g) {
-                    if (g % SCG == 0) {
+                    if (do_sc && g % SCG == 0) {
                         const int slot = (int)(isc % NSC);
                         if (!(ok = wait_bar<false>(B.empty_sc + 8 * slot, ((isc / NSC) & 1) ^ 1, abort))) break;
                         const uint32_t dst = sbase + OFF_SC + slot * SC_STAGE;
@@ -506,7 +519,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                                         B.full_sc + 8 * slot);
                         ++isc;
                     }
-                    if (kGrouped && g % GB == 0) {
+                    if (do_b && g % GB == 0) {
                         const int slot = (int)(ib % NB);
                         if (!(ok = wait_bar<false>(B.empty_b + 8 * slot, ((ib / NB) & 1) ^ 1, abort))) break;
                         mbar_expect_tx(B.full_b + 8 * slot, B_STAGE);
@@ -514,7 +527,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                                     (int32_t)T.bn0, B.full_b + 8 * slot);
                         ++ib;
                     }
-                    if (g % GA == 0) {
+                    if (do_a && g % GA == 0) {
                         const int slot = (int)(ia % NO);
                         if (!(ok = wait_bar<false>(B.done + 8 * slot, ((ia / NO) & 1) ^ 1, abort))) break;
                         mbar_expect_tx(B.full_a + 8 * slot, kGrouped ? A_STAGE : A_STAGE + F16_PAIR);
