@@ -617,9 +617,20 @@ def next_rows_section(dev, peaks, reps=20):
     ms = timeit(lambda: qg.kv3_decode(ck, sk, Dk))
     out["kv3_decode"] = {"shape": f"T={Tk} D={Dk}", "ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
     del xk, ck, sk
+    # The same byte count moved by a plain device copy (half read, half written),
+    # timed the same way: at 70-150 MB a call, launch and ramp take a visible part
+    # of any kernel, so this is the bound a streaming kernel of that size meets.
     for v in out.values():
+        half = (int(v["gbs"] * 1e9 * v["ms"] * 1e-3) // 2 + 15) // 16 * 16
+        src = torch.empty(half, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        v["copy_ms"] = timeit(lambda: dst.copy_(src))
+        v["frac_of_copy"] = v["copy_ms"] / v["ms"]
         v["frac_of_hbm"] = v["gbs"] / peaks["hbm_gbs"]
+        del src, dst
     out["l2"] = "flushed before every timed call"
+    out["copy"] = ("frac_of_copy: a device-to-device copy of the same bytes (half read, half "
+                   "written), timed the same way, divided by the kernel's time")
     del scrub
     return out
 
@@ -647,6 +658,7 @@ def flatten_sections(line, peaks, clocks):
     for k, v in line["next_rows"].items():
         if isinstance(v, dict):
             flat[f"next_{k}_frac"] = v["frac_of_hbm"]
+            flat[f"next_{k}_frac_of_copy"] = v["frac_of_copy"]
     for sec, clk in clocks.items():
         flat[f"{sec}_sm_mhz"] = clk.get("sm_mhz")
         flat[f"{sec}_clock_samples"] = clk.get("samples", 0)

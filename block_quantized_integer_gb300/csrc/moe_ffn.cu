@@ -106,6 +106,7 @@ swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t 
 }
 
 // One thread per 4 consecutive outputs of a token row (vec) or per output.
+constexpr int kSlots = 8;
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t T, int topk,
                int64_t N, float* __restrict__ out, bool vec4) {
@@ -117,14 +118,32 @@ combine_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t
         const float* wt = w + t * topk;
         const float* yt = y + t * topk * N;
         if (vec4) {
+            // the first kSlots slots' loads all go out before the first FMA;
+            // the sum still runs over the slots in order
+            float4 v[kSlots];
+            float ws[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+                if (s < topk) {
+                    ws[s] = wt[s];
+                    v[s] = *reinterpret_cast<const float4*>(yt + s * N + 4 * c);
+                }
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < topk; ++s) {
-                const float ws = wt[s];
-                const float4 v = *reinterpret_cast<const float4*>(yt + s * N + 4 * c);
-                acc.x = fmaf(ws, v.x, acc.x);
-                acc.y = fmaf(ws, v.y, acc.y);
-                acc.z = fmaf(ws, v.z, acc.z);
-                acc.w = fmaf(ws, v.w, acc.w);
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+                if (s < topk) {
+                    acc.x = fmaf(ws[s], v[s].x, acc.x);
+                    acc.y = fmaf(ws[s], v[s].y, acc.y);
+                    acc.z = fmaf(ws[s], v[s].z, acc.z);
+                    acc.w = fmaf(ws[s], v[s].w, acc.w);
+                }
+            for (int s = kSlots; s < topk; ++s) {
+                const float w1 = wt[s];
+                const float4 v1 = *reinterpret_cast<const float4*>(yt + s * N + 4 * c);
+                acc.x = fmaf(w1, v1.x, acc.x);
+                acc.y = fmaf(w1, v1.y, acc.y);
+                acc.z = fmaf(w1, v1.z, acc.z);
+                acc.w = fmaf(w1, v1.w, acc.w);
             }
             *reinterpret_cast<float4*>(out + t * N + 4 * c) = acc;
         } else {

@@ -42,13 +42,14 @@ def test_flatten_sections_keeps_scalars():
                     "down": {"ms": 0.2}},
             "moe_layer": {"total_ms": 0.65, "frac_of_hbm_weights": 0.1},
             "decode_m4": {"gbs": 4600.0},
-            "next_rows": {"kv3_encode": {"frac_of_hbm": 0.5}, "l2": "flushed"}}
+            "next_rows": {"kv3_encode": {"frac_of_hbm": 0.5, "frac_of_copy": 0.8}, "l2": "flushed"}}
     clk = {"sm_mhz": 2070.0, "samples": 12, "reasons": []}
     bench.flatten_sections(line, {"hbm_gbs": 6680.8},
                            {"prefill": clk, "longctx": clk, "moe": clk, "decode_m4": clk})
     for k in ("prefill_2048x12288x4096_tops", "prefill_2048x4096x12288_tops",
               "longctx_18432x17408x5120_tops", "longctx_18432x5120x17408_tops", "moe_total_ms",
-              "prefill_sm_mhz", "moe_throttle", "decode_m4_frac", "next_kv3_encode_frac"):
+              "prefill_sm_mhz", "moe_throttle", "decode_m4_frac", "next_kv3_encode_frac",
+              "next_kv3_encode_frac_of_copy"):
         assert k in line and k in line["prefill"], k
         assert not isinstance(line[k], (list, dict))
     assert line["clocks"]["prefill_reasons"] == "none"
