@@ -441,7 +441,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int G = (int)(K / kGroup);                    // multiple of 8
     const int PAIRS = G / 2;
     constexpr int GB = kQ4 ? 8 : 4;                      // groups per B stage
-    const int num_tiles = kGrouped ? ga.tile_offsets[ga.E] * n_tiles : (int)dense_tiles;
     const int t0 = blockIdx.x, dt = gridDim.x;
 
     if (tid == 0) {
@@ -480,6 +479,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched as a programmatic dependent of the pre-pass: barrier setup and the
+    // TMEM allocation above overlap its end; everything below may read its output
+    pdl_wait();
+    const int num_tiles = kGrouped ? ga.tile_offsets[ga.E] * n_tiles : (int)dense_tiles;
 
     const bool producer = warp == PROD_WARP || (kGrouped && (warp == BPROD_WARP || warp == SPROD_WARP));
     if (producer) {
@@ -833,6 +836,8 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
                   int64_t K, __half* __restrict__ a16, float* __restrict__ dxg,
                   const int32_t* __restrict__ perm, const int32_t* __restrict__ n_rows,
                   int32_t topk, int32_t x_row_mode) {
+    pdl_wait();                                      // the codes may come from the previous kernel
+    pdl_release();
     const int64_t chunks = K / 16;                   // 16 codes per thread step
     const int64_t G = K / kGroup;
     const int64_t limit = n_rows ? (int64_t)*n_rows : rows;
@@ -860,6 +865,8 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
 // nibble, each stored q + 8), written as 64 bytes of binary16 in element order.
 __global__ void __launch_bounds__(256)
 widen_q4_kernel(const uint8_t* __restrict__ qw4, int64_t groups, __half* __restrict__ w16) {
+    pdl_wait();
+    pdl_release();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < groups;
          i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 v = *reinterpret_cast<const uint4*>(qw4 + i * 16);
@@ -892,6 +899,8 @@ __global__ void __launch_bounds__(256)
 transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t N, int64_t G,
                         float* __restrict__ dwt, int64_t ldt) {
     __shared__ float tile[32][33];                       // [column][group], padded
+    pdl_wait();
+    pdl_release();
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int64_t n0 = (int64_t)blockIdx.x * 32, g0 = (int64_t)blockIdx.y * 32;
     for (int i = ty; i < 32; i += 8) {                   // column n0 + i, group g0 + tx
@@ -942,6 +951,8 @@ __global__ void __launch_bounds__(1024)
 tile_info_kernel(const int32_t* __restrict__ offsets, int32_t E, int4* __restrict__ info) {
     __shared__ int32_t part[3][32];
     __shared__ int32_t run[3];
+    pdl_wait();                                          // offsets come from the routing kernel
+    pdl_release();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     // tiles of expert e per class: full tiles and a tail of > 64 rows in
     // class 0, a shorter tail in class 1 or 2
@@ -1097,10 +1108,9 @@ cudaError_t launch_kernel(dim3 grid, const CUtensorMap& ma, const CUtensorMap& m
                                      9 + (kQ4 ? 1 : 0) + (kGrouped ? 2 : 0));
     if (e != cudaSuccess) return e;
     const bool vec2 = ((uintptr_t)y % 8 == 0) && (ldy % 2 == 0);
-    tc_gemm_kernel<kQ4, kGrouped><<<grid, kGrouped ? THREADS : THREADS_DENSE, SMEM_BYTES, s>>>(ma, mb, mdx, mdw, y, M, N, K,
-                                                                    ldy, vec2, ga, n_tiles,
-                                                                    dense_tiles, ta);
-    return cudaGetLastError();
+    return launch_pdl(tc_gemm_kernel<kQ4, kGrouped>, grid, dim3(kGrouped ? THREADS : THREADS_DENSE),
+                      (size_t)SMEM_BYTES, s, ma, mb, mdx, mdw, y, M, N, K, ldy, vec2, ga, n_tiles,
+                      dense_tiles, ta);
 }
 
 // Tail split of a dense product with `tiles` output tiles and G groups: the
@@ -1176,16 +1186,21 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     const size_t off_part = off_w16 + align16((size_t)N * K * 2);
     float* dwt = reinterpret_cast<float*>(ws + off_dwt);
     __half* w16 = reinterpret_cast<__half*>(ws + off_w16);
-    widen_rows_kernel<<<widen_grid(M * (K / 16)), 256, 0, s>>>(qx, dx, M, K, a16, nullptr, nullptr,
-                                                               nullptr, 1, 0);
-    if (q4)
-        widen_q4_kernel<<<widen_grid(N * G), 256, 0, s>>>(static_cast<const uint8_t*>(qw), N * G, w16);
-    else
-        widen_rows_kernel<<<widen_grid(N * (K / 16)), 256, 0, s>>>(
-            static_cast<const int8_t*>(qw), nullptr, N, K, w16, nullptr, nullptr, nullptr, 1, 0);
-    transpose_scales_kernel<<<dim3((unsigned)(ldt / 32), (unsigned)((G + 31) / 32)), 256, 0, s>>>(
-        dw, N, G, dwt, ldt);
-    cudaError_t e = cudaGetLastError();
+    // the pre-pass kernels and the GEMM form a chain of programmatic dependent
+    // launches: each waits for its predecessor before reading, so a launch and
+    // its set-up overlap the end of the kernel before it
+    cudaError_t e = launch_pdl(widen_rows_kernel, dim3(widen_grid(M * (K / 16))), dim3(256), 0, s, qx, dx,
+                               M, K, a16, (float*)nullptr, (const int32_t*)nullptr,
+                               (const int32_t*)nullptr, 1, 0);
+    if (e != cudaSuccess) return e;
+    e = q4 ? launch_pdl(widen_q4_kernel, dim3(widen_grid(N * G)), dim3(256), 0, s,
+                        static_cast<const uint8_t*>(qw), N * G, w16)
+           : launch_pdl(widen_rows_kernel, dim3(widen_grid(N * (K / 16))), dim3(256), 0, s,
+                        static_cast<const int8_t*>(qw), (const float*)nullptr, N, K, w16, (float*)nullptr,
+                        (const int32_t*)nullptr, (const int32_t*)nullptr, 1, 0);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(transpose_scales_kernel, dim3((unsigned)(ldt / 32), (unsigned)((G + 31) / 32)), dim3(256),
+                   0, s, dw, N, G, dwt, ldt);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, w16, dx, dwt, M, N, ldt, K, q4))
@@ -1229,10 +1244,10 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     float* dxg = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2));
     int4* info = reinterpret_cast<int4*>(ws + align16((size_t)P * K * 2) + align16((size_t)P * G * 4));
     // gather + widen the routed rows (count read on the device: offsets[E])
-    widen_rows_kernel<<<widen_grid(P * (K / 16)), 256, 0, s>>>(qx, dx, P, K, a16, dxg, perm,
-                                                               offsets + E, topk, x_row_mode);
-    tile_info_kernel<<<1, 1024, 0, s>>>(offsets, E, info);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(widen_rows_kernel, dim3(widen_grid(P * (K / 16))), dim3(256), 0, s, qx, dx,
+                               P, K, a16, dxg, perm, offsets + E, topk, x_row_mode);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(tile_info_kernel, dim3(1), dim3(1024), 0, s, offsets, E, info);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dw, P, (int64_t)E * N, 0, K, true))

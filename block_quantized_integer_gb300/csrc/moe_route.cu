@@ -13,7 +13,7 @@
 // (optional), counting them in *d_err without trapping.
 //
 // Stability without a global sort: warp w owns the contiguous slice w of the
-// pairs.  Phase 1 counts experts per warp; phase 2 turns the per-warp counts
+// pairs (read from a shared-memory copy of the ids when they fit).  Phase 1 counts experts per warp; phase 2 turns the per-warp counts
 // into starting positions (expert-major, then warp order); phase 3 walks each
 // slice in order 32 pairs at a time, ranks equal experts inside the step with
 // __match_any_sync, and advances the warp's private cursor of each expert.
@@ -26,26 +26,51 @@ namespace {
 
 constexpr int kRouteWarps = 16;
 constexpr int kMaxExperts = 1024;
+constexpr int64_t kStageMax = 32768;      // routed pairs whose ids are staged in shared memory
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
 moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ perm, int32_t* __restrict__ tile_offsets, int bm,
                  float* __restrict__ y, int64_t N, int32_t* __restrict__ d_err) {
-    extern __shared__ int32_t cnt[];          // [kRouteWarps][E] then scan [E+1]
+    extern __shared__ int32_t cnt[];          // [kRouteWarps][E], scans [E+1] x 2, staged ids [P]
     int32_t* scan = cnt + kRouteWarps * E;
     int32_t* tscan = scan + (E + 1);
+    int32_t* sid = tscan + (E + 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t L = (P + kRouteWarps - 1) / kRouteWarps;
     const int64_t s0 = min64(P, warp * L), s1 = min64(P, s0 + L);
+    pdl_wait();                               // the ids may come from the previous kernel
+    pdl_release();
 
+    // Up to kStageMax pairs, the ids are first copied into shared memory by
+    // the whole block, four loads in flight a thread: both walks over a warp's
+    // slice then read shared memory instead of waiting on one global load per
+    // step.
+    const bool staged = P <= kStageMax;
+    if (staged) {
+        for (int64_t i0 = tid; i0 < P; i0 += 4 * (int64_t)blockDim.x) {
+            int32_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * (int64_t)blockDim.x;
+                v[u] = i < P ? ids[i] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * (int64_t)blockDim.x;
+                if (i < P) sid[i] = v[u];
+            }
+        }
+    }
+    const int32_t* src = staged ? sid : ids;
     for (int i = tid; i < kRouteWarps * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
 
     // phase 1: per-warp expert counts; unrouted pairs counted into d_err
     int bad = 0;
     for (int64_t p = s0 + lane; p < s1; p += 32) {
-        const int32_t e = ids[p];
+        const int32_t e = src[p];
         if (e >= 0 && e < E) atomicAdd(&cnt[warp * E + e], 1);
         else ++bad;
     }
@@ -103,7 +128,7 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
     const unsigned lt = (1u << lane) - 1u;
     for (int64_t base = s0; base < s1; base += 32) {
         const int64_t p = base + lane;
-        int32_t e = p < s1 ? ids[p] : -1;
+        int32_t e = p < s1 ? src[p] : -1;
         const bool ok = e >= 0 && e < E;
         if (!ok) e = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -127,13 +152,12 @@ cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, i
                              int32_t* tile_offsets, int bm, float* y, int64_t N,
                              int32_t* d_err, cudaStream_t s) {
     if (E > kMaxExperts) return cudaErrorInvalidValue;
-    const int smem = (kRouteWarps * E + 2 * (E + 1)) * 4;
+    const int64_t P = T * topk;
+    const int smem = (int)((kRouteWarps * E + 2 * (E + 1) + (P <= kStageMax ? P : 0)) * 4);
     cudaError_t e = ensure_smem_attr((const void*)moe_route_kernel, smem, 8);
     if (e != cudaSuccess) return e;
-    moe_route_kernel<<<1, kRouteWarps * 32, smem, s>>>(topk_ids, T * topk, E, counts, offsets,
-                                                        perm, tile_offsets, bm < 1 ? 1 : bm, y,
-                                                        N, d_err);
-    return cudaGetLastError();
+    return launch_pdl(moe_route_kernel, dim3(1), dim3(kRouteWarps * 32), (size_t)smem, s, topk_ids, P,
+                      E, counts, offsets, perm, tile_offsets, bm < 1 ? 1 : bm, y, N, d_err);
 }
 
 }  // namespace qg
