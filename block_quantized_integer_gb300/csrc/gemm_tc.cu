@@ -819,6 +819,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           }
         }
 
+    // this CTA's tiles are done: the next kernel on the stream may start
+    // launching (it still waits for the whole grid before it reads anything)
+    pdl_release();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -828,22 +831,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 }
 
 // ---- pre-pass: int8 codes -> binary16 (optionally gathered) ---------------------------
+//
+// Each step is written as the work of block blk of nblk blocks (a grid-stride
+// range), so that the dense product can run all three of its steps in one
+// launch (dense_prepass_kernel) and the grouped product its gather alone.
 
 // Dense: a16[r] = fp16(qx[r]).  Grouped (perm != nullptr): sorted position i
 // takes activation row x_row(perm[i]); its scales are gathered into dxg too.
-__global__ void __launch_bounds__(256)
-widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, int64_t rows,
-                  int64_t K, __half* __restrict__ a16, float* __restrict__ dxg,
-                  const int32_t* __restrict__ perm, const int32_t* __restrict__ n_rows,
-                  int32_t topk, int32_t x_row_mode) {
-    pdl_wait();                                      // the codes may come from the previous kernel
-    pdl_release();
+__device__ __forceinline__ void widen_rows_range(const int8_t* __restrict__ qx, const float* __restrict__ dx,
+                                                 int64_t rows, int64_t K, __half* __restrict__ a16,
+                                                 float* __restrict__ dxg, const int32_t* __restrict__ perm,
+                                                 const int32_t* __restrict__ n_rows, int32_t topk,
+                                                 int32_t x_row_mode, int64_t blk, int64_t nblk) {
     const int64_t chunks = K / 16;                   // 16 codes per thread step
     const int64_t G = K / kGroup;
     const int64_t limit = n_rows ? (int64_t)*n_rows : rows;
     const int64_t total = limit * chunks;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t i = blk * blockDim.x + threadIdx.x; i < total; i += nblk * blockDim.x) {
         const int64_t r = i / chunks, c = i % chunks;
         int64_t src = r;
         if (perm) {
@@ -863,12 +867,9 @@ widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, i
 // Dense Q4 weights -> binary16 [N][K]: one packed 16-byte group per thread
 // step (byte j: element j in the low nibble, element j + 16 in the high
 // nibble, each stored q + 8), written as 64 bytes of binary16 in element order.
-__global__ void __launch_bounds__(256)
-widen_q4_kernel(const uint8_t* __restrict__ qw4, int64_t groups, __half* __restrict__ w16) {
-    pdl_wait();
-    pdl_release();
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < groups;
-         i += (int64_t)gridDim.x * blockDim.x) {
+__device__ __forceinline__ void widen_q4_range(const uint8_t* __restrict__ qw4, int64_t groups,
+                                               __half* __restrict__ w16, int64_t blk, int64_t nblk) {
+    for (int64_t i = blk * blockDim.x + threadIdx.x; i < groups; i += nblk * blockDim.x) {
         const uint4 v = *reinterpret_cast<const uint4*>(qw4 + i * 16);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t lo_h[8], hi_h[8];
@@ -892,17 +893,15 @@ widen_q4_kernel(const uint8_t* __restrict__ qw4, int64_t groups, __half* __restr
 // group-major binary32 rows of ldt columns (ldt a multiple of 32), the layout
 // the epilogue reads.  Inside each 32-column block, column 8j + 2c + e is
 // stored at 8c + 2j + e (j, c < 4, e < 2), so the 8 columns one epilogue
-// thread scales are contiguous; columns past N are stored as zero.  A block
-// takes 32 columns x 32 groups: dw rows are read along g into shared memory,
-// then dwT rows are written along the stored column (both coalesced).
-__global__ void __launch_bounds__(256)
-transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t N, int64_t G,
-                        float* __restrict__ dwt, int64_t ldt) {
-    __shared__ float tile[32][33];                       // [column][group], padded
-    pdl_wait();
-    pdl_release();
+// thread scales are contiguous; columns past N are stored as zero.  One tile
+// (bx, by) is 32 columns x 32 groups: dw rows are read along g into shared
+// memory, then dwT rows are written along the stored column (both coalesced).
+// Every thread of the block calls it (it synchronises the block).
+__device__ __forceinline__ void transpose_scales_tile(const uint16_t* __restrict__ dw, int64_t N, int64_t G,
+                                                      float* __restrict__ dwt, int64_t ldt, int64_t bx,
+                                                      int64_t by, float (&tile)[32][33]) {
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t n0 = (int64_t)blockIdx.x * 32, g0 = (int64_t)blockIdx.y * 32;
+    const int64_t n0 = bx * 32, g0 = by * 32;
     for (int i = ty; i < 32; i += 8) {                   // column n0 + i, group g0 + tx
         const int64_t n = n0 + i, g = g0 + tx;
         tile[i][tx] = (n < N && g < G) ? half_bits_to_float(dw[n * G + g]) : 0.f;
@@ -917,11 +916,63 @@ transpose_scales_kernel(const uint16_t* __restrict__ dw, int64_t N, int64_t G,
     }
 }
 
+// The grouped product's gather (and any single widening).
+__global__ void __launch_bounds__(256)
+widen_rows_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx, int64_t rows,
+                  int64_t K, __half* __restrict__ a16, float* __restrict__ dxg,
+                  const int32_t* __restrict__ perm, const int32_t* __restrict__ n_rows,
+                  int32_t topk, int32_t x_row_mode) {
+    pdl_wait();                                      // the codes may come from the previous kernel
+    pdl_release();
+    widen_rows_range(qx, dx, rows, K, a16, dxg, perm, n_rows, topk, x_row_mode, blockIdx.x, gridDim.x);
+}
+
+// The dense product's pre-pass in one launch: blocks [0, nb_w) widen the
+// weight codes, the next nb_a the activation codes, the rest transpose one
+// 32 x 32 tile of the weight scales each.  The three steps touch disjoint
+// buffers, so they share the HBM bandwidth instead of running one after
+// another (and two launch gaps are gone).
+struct DensePrepass {
+    const int8_t* qx;            // activation codes [M][K]
+    __half* a16;
+    const void* qw;              // weight codes [N][K] (Q8) or [N][K/2] (Q4)
+    __half* w16;
+    const uint16_t* dw;          // weight scales [N][G]
+    float* dwt;                  // [G][ldt]
+    int64_t M, N, K, G, ldt;
+    int nb_w, nb_a, tiles_x;     // blocks per step; scale tiles along N
+    bool q4;
+};
+
+__global__ void __launch_bounds__(256)
+dense_prepass_kernel(const DensePrepass a) {
+    __shared__ float tile[32][33];
+    pdl_wait();                                      // the codes may come from the previous kernel
+    pdl_release();
+    int64_t b = blockIdx.x;
+    if (b < a.nb_w) {
+        if (a.q4)
+            widen_q4_range(static_cast<const uint8_t*>(a.qw), a.N * a.G, a.w16, b, a.nb_w);
+        else
+            widen_rows_range(static_cast<const int8_t*>(a.qw), nullptr, a.N, a.K, a.w16, nullptr, nullptr,
+                             nullptr, 1, 0, b, a.nb_w);
+        return;
+    }
+    b -= a.nb_w;
+    if (b < a.nb_a) {
+        widen_rows_range(a.qx, nullptr, a.M, a.K, a.a16, nullptr, nullptr, nullptr, 1, 0, b, a.nb_a);
+        return;
+    }
+    b -= a.nb_a;
+    transpose_scales_tile(a.dw, a.N, a.G, a.dwt, a.ldt, b % a.tiles_x, b / a.tiles_x, tile);
+}
+
 // y of the tail tiles: the sum of each tile's K-chunk partials, added in chunk
 // order (deterministic).  One thread per output element of the tail tiles.
 __global__ void __launch_bounds__(256)
 tail_reduce_kernel(const float* __restrict__ part, int full, int split, int tail_tiles,
                    int n_tiles, int64_t M, int64_t N, float* __restrict__ y, int64_t ldy) {
+    pdl_wait();                                          // the partial sums of the GEMM
     const int64_t total = (int64_t)tail_tiles * BM * BN;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -1186,21 +1237,22 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
     const size_t off_part = off_w16 + align16((size_t)N * K * 2);
     float* dwt = reinterpret_cast<float*>(ws + off_dwt);
     __half* w16 = reinterpret_cast<__half*>(ws + off_w16);
-    // the pre-pass kernels and the GEMM form a chain of programmatic dependent
-    // launches: each waits for its predecessor before reading, so a launch and
-    // its set-up overlap the end of the kernel before it
-    cudaError_t e = launch_pdl(widen_rows_kernel, dim3(widen_grid(M * (K / 16))), dim3(256), 0, s, qx, dx,
-                               M, K, a16, (float*)nullptr, (const int32_t*)nullptr,
-                               (const int32_t*)nullptr, 1, 0);
-    if (e != cudaSuccess) return e;
-    e = q4 ? launch_pdl(widen_q4_kernel, dim3(widen_grid(N * G)), dim3(256), 0, s,
-                        static_cast<const uint8_t*>(qw), N * G, w16)
-           : launch_pdl(widen_rows_kernel, dim3(widen_grid(N * (K / 16))), dim3(256), 0, s,
-                        static_cast<const int8_t*>(qw), (const float*)nullptr, N, K, w16, (float*)nullptr,
-                        (const int32_t*)nullptr, (const int32_t*)nullptr, 1, 0);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(transpose_scales_kernel, dim3((unsigned)(ldt / 32), (unsigned)((G + 31) / 32)), dim3(256),
-                   0, s, dw, N, G, dwt, ldt);
+    // the pre-pass and the GEMM are programmatic dependent launches: each
+    // waits for its predecessor before reading, so a launch and its set-up
+    // overlap the end of the kernel before it
+    const int sm = sm_count();
+    DensePrepass pa;
+    pa.qx = qx; pa.a16 = a16; pa.qw = qw; pa.w16 = w16; pa.dw = dw; pa.dwt = dwt;
+    pa.M = M; pa.N = N; pa.K = K; pa.G = G; pa.ldt = ldt; pa.q4 = q4;
+    const int64_t w_items = q4 ? N * G : N * (K / 16), a_items = M * (K / 16);
+    pa.nb_w = (int)min64((w_items + 255) / 256, (int64_t)sm * 4);
+    pa.nb_a = (int)min64((a_items + 255) / 256, (int64_t)sm * 2);
+    if (pa.nb_w < 1) pa.nb_w = 1;
+    if (pa.nb_a < 1) pa.nb_a = 1;
+    pa.tiles_x = (int)(ldt / 32);
+    const int64_t nb_t = (int64_t)pa.tiles_x * ((G + 31) / 32);
+    cudaError_t e = launch_pdl(dense_prepass_kernel, dim3((unsigned)(pa.nb_w + pa.nb_a + nb_t)), dim3(256), 0,
+                               s, pa);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, w16, dx, dwt, M, N, ldt, K, q4))
@@ -1218,9 +1270,8 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
            : launch_kernel<false, false>(grid, ma, mb, mdx, mdw, y, M, N, K, ldy, ga, n_tiles, units, ta, s);
     if (e != cudaSuccess || tp.tail == 0) return e;
     const int64_t elems = tp.tail * BM * BN;
-    tail_reduce_kernel<<<widen_grid(elems), 256, 0, s>>>(part, (int)tp.full, tp.split, (int)tp.tail,
-                                                         n_tiles, M, N, y, ldy);
-    return cudaGetLastError();
+    return launch_pdl(tail_reduce_kernel, dim3(widen_grid(elems)), dim3(256), 0, s, (const float*)part,
+                      (int)tp.full, tp.split, (int)tp.tail, n_tiles, M, N, y, ldy);
 }
 
 // MoE workspace after the routing tables: a16 [P][K] binary16 and dxg [P][G]

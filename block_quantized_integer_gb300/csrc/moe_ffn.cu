@@ -43,6 +43,8 @@ template <bool kFast>
 __global__ void __launch_bounds__(256)
 swiglu_quant_kernel(const float* __restrict__ gu, int64_t P, int64_t F, int64_t ldgu,
                     int8_t* __restrict__ qh, float* __restrict__ dh, bool vec_ok, FastDiv fg) {
+    pdl_wait();                               // gu comes from the gate/up GEMM
+    pdl_release();
     constexpr int U = 2;
     const int64_t G = F / kGroup;
     const int64_t total = P * G;
@@ -110,6 +112,8 @@ constexpr int kSlots = 8;
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t T, int topk,
                int64_t N, float* __restrict__ out, bool vec4) {
+    pdl_wait();                               // y comes from the down GEMM
+    pdl_release();
     const int64_t per_row = vec4 ? N / 4 : N;
     const int64_t total = T * per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -167,20 +171,19 @@ cudaError_t launch_swiglu_quant(const float* gu, int64_t P, int64_t F, int64_t l
                                 float* dh, cudaStream_t s) {
     const bool vec_ok = ((uintptr_t)gu % 16 == 0) && (ldgu % 4 == 0) && (F % 4 == 0);
     const int64_t total = P * (F / kGroup);
+    const dim3 grid(stream_grid(total * 8)), block(256);
     if (total < (1ll << 32))
-        swiglu_quant_kernel<true><<<stream_grid(total * 8), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok,
-                                                                       FastDiv((uint32_t)(F / kGroup)));
-    else
-        swiglu_quant_kernel<false><<<stream_grid(total * 8), 256, 0, s>>>(gu, P, F, ldgu, qh, dh, vec_ok,
-                                                                        FastDiv(1));
-    return cudaGetLastError();
+        return launch_pdl(swiglu_quant_kernel<true>, grid, block, 0, s, gu, P, F, ldgu, qh, dh, vec_ok,
+                          FastDiv((uint32_t)(F / kGroup)));
+    return launch_pdl(swiglu_quant_kernel<false>, grid, block, 0, s, gu, P, F, ldgu, qh, dh, vec_ok,
+                      FastDiv(1));
 }
 
 cudaError_t launch_combine(const float* y, const float* w, int64_t T, int topk, int64_t N,
                            float* out, cudaStream_t s) {
     const bool vec4 = (N % 4 == 0) && ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
-    combine_kernel<<<stream_grid(T * (vec4 ? N / 4 : N)), 256, 0, s>>>(y, w, T, topk, N, out, vec4);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(stream_grid(T * (vec4 ? N / 4 : N))), dim3(256), 0, s, y, w, T,
+                      topk, N, out, vec4);
 }
 
 }  // namespace qg
