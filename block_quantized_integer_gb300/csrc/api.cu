@@ -255,7 +255,7 @@ qg_status moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
          (uintptr_t)d_err) & 3u)
         return QG_ERR_ALIGNMENT;
     return from_cuda(qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, nullptr,
-                                          1, nullptr, 0, d_err, stream));
+                                          1, nullptr, nullptr, 0, d_err, stream));
 }
 
 qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, int64_t K,
@@ -284,8 +284,9 @@ qg_status grouped_qgemm_moe(const int8_t* qx, const float* dx, int64_t rows_x, i
     int32_t* tiles = (int32_t*)(ws + w.tiles);
     int32_t* perm = (int32_t*)(ws + w.perm);
     const int bm = tc ? qg::tc_tile_m() : qg::mma_tile_m();
+    int4* table = tc ? qg::tc_grouped_tile_table(ws + w.total, P, K) : nullptr;
     cudaError_t e = qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, tiles, bm,
-                                         y, N, d_err, stream);
+                                         table, y, N, d_err, stream);
     if (e != cudaSuccess) return QG_ERR_CUDA;
     if (tc)
         return from_cuda(qg::launch_tc_grouped(qx, dx, P, N, K, qw4, dw, y, E, topk, x_row_mode,

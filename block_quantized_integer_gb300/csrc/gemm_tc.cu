@@ -996,98 +996,6 @@ tail_reduce_kernel(const float* __restrict__ part, int full, int split, int tail
 // twice per call (each change drains the pair-slot ring).  Each entry:
 // {first sorted row, rows, expert, 0}; the entry count equals tile_offsets[E].
 // One block of 1024 threads, experts taken 1024 at a time.
-__device__ __forceinline__ int width_class(int32_t rows) { return rows > 64 ? 0 : (rows > 32 ? 1 : 2); }
-
-__global__ void __launch_bounds__(1024)
-tile_info_kernel(const int32_t* __restrict__ offsets, int32_t E, int4* __restrict__ info) {
-    __shared__ int32_t part[3][32];
-    __shared__ int32_t run[3];
-    pdl_wait();                                          // offsets come from the routing kernel
-    pdl_release();
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    // tiles of expert e per class: full tiles and a tail of > 64 rows in
-    // class 0, a shorter tail in class 1 or 2
-    auto counts = [&](int e, int32_t (&c)[3]) {
-        c[0] = c[1] = c[2] = 0;
-        if (e >= E) return;
-        const int32_t n = offsets[e + 1] - offsets[e], tail = n % BM;
-        c[0] = n / BM;
-        if (tail > 0) ++c[width_class(tail)];
-    };
-    // exclusive block scan of c (per class); returns the chunk totals in tot
-    auto block_scan = [&](int32_t (&c)[3], int32_t (&ex)[3], int32_t (&tot)[3]) {
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            int32_t v = c[k];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            if (lane == 31) part[k][wid] = v;
-            ex[k] = v - c[k];
-        }
-        __syncthreads();
-        if (wid == 0) {
-#pragma unroll
-            for (int k = 0; k < 3; ++k) {
-                int32_t v = part[k][lane];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                part[k][lane] = v;                      // inclusive over warps
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            ex[k] += wid > 0 ? part[k][wid - 1] : 0;
-            tot[k] = part[k][31];
-        }
-        __syncthreads();                                // part reused by the next chunk
-    };
-    // pass 1: class sizes
-    int32_t size[3] = {0, 0, 0};
-    for (int e0 = 0; e0 < E; e0 += 1024) {
-        int32_t c[3], ex[3], tot[3];
-        counts(e0 + tid, c);
-        block_scan(c, ex, tot);
-#pragma unroll
-        for (int k = 0; k < 3; ++k) size[k] += tot[k];
-    }
-    if (tid == 0) {
-        run[0] = 0;
-        run[1] = size[0];
-        run[2] = size[0] + size[1];
-    }
-    __syncthreads();
-    // pass 2: placement
-    for (int e0 = 0; e0 < E; e0 += 1024) {
-        const int e = e0 + tid;
-        int32_t c[3], ex[3], tot[3];
-        counts(e, c);
-        block_scan(c, ex, tot);
-        if (e < E) {
-            const int32_t first = offsets[e], end = offsets[e + 1];
-            int32_t m0 = first;
-            int32_t at = run[0] + ex[0];
-            for (; end - m0 > 64; m0 += BM) info[at++] = make_int4(m0, min(BM, end - m0), e, 0);
-            if (end > m0) {
-                const int k = width_class(end - m0);
-                info[run[k] + ex[k]] = make_int4(m0, end - m0, e, 0);
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-#pragma unroll
-            for (int k = 0; k < 3; ++k) run[k] += tot[k];
-        }
-        __syncthreads();
-    }
-}
-
 // ---- host side ----------------------------------------------------------------------
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1277,6 +1185,12 @@ cudaError_t launch_tc_gemm(const int8_t* qx, const float* dx, int64_t M, int64_t
 // MoE workspace after the routing tables: a16 [P][K] binary16 and dxg [P][G]
 // binary32 (gathered activation rows and scales in expert order), and the
 // m-tile table (at most P / 128 + E tiles, 16 bytes each).
+int4* tc_grouped_tile_table(void* workspace, int64_t P, int64_t K) {
+    const int64_t G = K / kGroup;
+    return reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + align16((size_t)P * K * 2) +
+                                   align16((size_t)P * G * 4));
+}
+
 size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E) {
     (void)N;
     const int64_t G = K / kGroup;
@@ -1293,12 +1207,10 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* a16 = reinterpret_cast<__half*>(ws);
     float* dxg = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2));
-    int4* info = reinterpret_cast<int4*>(ws + align16((size_t)P * K * 2) + align16((size_t)P * G * 4));
+    int4* info = tc_grouped_tile_table(workspace, P, K);      // filled by the routing kernel
     // gather + widen the routed rows (count read on the device: offsets[E])
     cudaError_t e = launch_pdl(widen_rows_kernel, dim3(widen_grid(P * (K / 16))), dim3(256), 0, s, qx, dx,
                                P, K, a16, dxg, perm, offsets + E, topk, x_row_mode);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(tile_info_kernel, dim3(1), dim3(1024), 0, s, offsets, E, info);
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb, mdx, mdw;
     if (!make_maps(&ma, &mb, &mdx, &mdw, a16, qw4, dxg, dw, P, (int64_t)E * N, 0, K, true))

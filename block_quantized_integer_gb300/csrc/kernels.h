@@ -52,6 +52,8 @@ unsigned int read_and_clear_tc_error();
 cudaError_t set_wait_limit(long long cycles);
 int tc_tile_m();
 size_t tc_grouped_workspace(int64_t P, int64_t N, int64_t K, int32_t E);
+// Where the m-tile table lies in that workspace (the routing kernel fills it).
+int4* tc_grouped_tile_table(void* workspace, int64_t P, int64_t K);
 cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int64_t N, int64_t K,
                               const uint8_t* qw4, const uint16_t* dw, float* y, int32_t E,
                               int32_t topk, int32_t x_row_mode, const int32_t* perm,
@@ -59,10 +61,11 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
                               void* workspace, cudaStream_t s);
 
 // Routing: counts/offsets/perm (+ m-tile offsets for tile height bm when
-// tile_offsets != nullptr; + zeroing of unrouted rows of y when y != nullptr).
+// tile_offsets != nullptr; + the tensor-core GEMM's m-tile table when
+// tile_table != nullptr; + zeroing of unrouted rows of y when y != nullptr).
 cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                              int32_t* counts, int32_t* offsets, int32_t* perm,
-                             int32_t* tile_offsets, int bm, float* y, int64_t N,
+                             int32_t* tile_offsets, int bm, int4* tile_table, float* y, int64_t N,
                              int32_t* d_err, cudaStream_t s);
 
 // MoE steps around the grouped GEMM.

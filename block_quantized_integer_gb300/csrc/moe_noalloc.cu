@@ -94,7 +94,7 @@ extern "C" qg_status grouped_qgemm_moe_noalloc(const int8_t* qx, const float* dx
     int32_t* tiles = reinterpret_cast<int32_t*>(ws + kTilesOff);
     int32_t* perm = reinterpret_cast<int32_t*>(ws + kPermOff);
     e = qg::launch_moe_route(topk_ids, T, topk, E, counts, offsets, perm, tiles,
-                             qg::mma_tile_m(), y, N, d_err, stream);
+                             qg::mma_tile_m(), nullptr, y, N, d_err, stream);
     if (e != cudaSuccess) return QG_ERR_CUDA;
     qg::GatherArgs ga{perm, offsets, tiles, E, topk, x_row_mode};
     e = qg::launch_mma_grouped(qx, dx, P, N, K, qw4, dw, y, ga, stream);

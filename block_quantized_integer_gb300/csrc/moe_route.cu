@@ -3,12 +3,13 @@
 // grouped 4-bit GEMM for MoE routing during prefill).
 //
 // From topk_ids [T][topk] (pairs p = token * topk + slot) it builds, in one
-// block of 16 warps:
+// block of 32 warps:
 //   counts[e]        pairs routed to expert e,
 //   offsets[e]       exclusive prefix sum of counts (offsets[E] = routed pairs),
 //   perm[...]        pair indices grouped by expert, (token, slot) order inside
 //                    an expert (a stable counting sort),
 //   tile_offsets[e]  exclusive prefix sum of ceil(counts[e] / bm) (optional),
+//   the m-tile table of the tensor-core grouped GEMM (optional),
 // and zeroes the output rows of pairs whose expert id is out of range
 // (optional), counting them in *d_err without trapping.
 //
@@ -24,15 +25,107 @@ namespace qg {
 
 namespace {
 
-constexpr int kRouteWarps = 16;
+constexpr int kRouteWarps = 32;
 constexpr int kMaxExperts = 1024;
-constexpr int64_t kStageMax = 32768;      // routed pairs whose ids are staged in shared memory
+constexpr int64_t kStageBytes = 160 * 1024;   // shared memory the ids may be staged in, with the counts
+
+__device__ __forceinline__ int width_class(int32_t rows) { return rows > 64 ? 0 : (rows > 32 ? 1 : 2); }
+
+// The m-tile table of the tensor-core grouped GEMM, from the exclusive offsets
+// off[0..E] (shared memory): per expert its full bm-row tiles and a tail of
+// more than 64 rows in class 0, a shorter tail in class 1 (33-64 rows) or 2
+// (at most 32), the classes one after another and each in expert order;
+// entry {first sorted row, rows, expert, 0}.  Tiles of one width class then
+// follow each other in the GEMM's tile order.  The whole block calls it.
+__device__ void build_tile_table(const int32_t* __restrict__ off, int32_t E, int bm, int4* __restrict__ table) {
+    __shared__ int32_t part[3][32];
+    __shared__ int32_t run[3];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    auto counts = [&](int e, int32_t (&c)[3]) {
+        c[0] = c[1] = c[2] = 0;
+        if (e >= E) return;
+        const int32_t n = off[e + 1] - off[e], tail = n % bm;
+        c[0] = n / bm;
+        if (tail > 0) ++c[width_class(tail)];
+    };
+    // exclusive block scan of c per class; tot = the chunk's totals
+    auto block_scan = [&](int32_t (&c)[3], int32_t (&ex)[3], int32_t (&tot)[3]) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            int32_t v = c[k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane == 31) part[k][wid] = v;
+            ex[k] = v - c[k];
+        }
+        __syncthreads();
+        if (wid == 0) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                int32_t v = lane < nw ? part[k][lane] : 0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                part[k][lane] = v;                      // inclusive over warps
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            ex[k] += wid > 0 ? part[k][wid - 1] : 0;
+            tot[k] = part[k][31];
+        }
+        __syncthreads();                                // part is reused by the next chunk
+    };
+    int32_t size[3] = {0, 0, 0};                        // pass 1: class sizes
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        int32_t c[3], ex[3], tot[3];
+        counts(e0 + tid, c);
+        block_scan(c, ex, tot);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) size[k] += tot[k];
+    }
+    if (tid == 0) {
+        run[0] = 0;
+        run[1] = size[0];
+        run[2] = size[0] + size[1];
+    }
+    __syncthreads();
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {          // pass 2: placement
+        const int e = e0 + tid;
+        int32_t c[3], ex[3], tot[3];
+        counts(e, c);
+        block_scan(c, ex, tot);
+        if (e < E) {
+            const int32_t first = off[e], end = off[e + 1];
+            int32_t m0 = first;
+            int32_t at = run[0] + ex[0];
+            for (; end - m0 > 64; m0 += bm) table[at++] = make_int4(m0, min(bm, end - m0), e, 0);
+            if (end > m0) {
+                const int k = width_class(end - m0);
+                table[run[k] + ex[k]] = make_int4(m0, end - m0, e, 0);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) run[k] += tot[k];
+        }
+        __syncthreads();
+    }
+}
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
 moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ perm, int32_t* __restrict__ tile_offsets, int bm,
-                 float* __restrict__ y, int64_t N, int32_t* __restrict__ d_err) {
+                 int4* __restrict__ table, float* __restrict__ y, int64_t N,
+                 int32_t* __restrict__ d_err, bool staged) {
     extern __shared__ int32_t cnt[];          // [kRouteWarps][E], scans [E+1] x 2, staged ids [P]
     int32_t* scan = cnt + kRouteWarps * E;
     int32_t* tscan = scan + (E + 1);
@@ -43,11 +136,9 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
     pdl_wait();                               // the ids may come from the previous kernel
     pdl_release();
 
-    // Up to kStageMax pairs, the ids are first copied into shared memory by
-    // the whole block, four loads in flight a thread: both walks over a warp's
-    // slice then read shared memory instead of waiting on one global load per
-    // step.
-    const bool staged = P <= kStageMax;
+    // When they fit, the ids are first copied into shared memory by the whole
+    // block, four loads in flight a thread: both walks over a warp's slice then
+    // read shared memory instead of waiting on one global load per step.
     if (staged) {
         for (int64_t i0 = tid; i0 < P; i0 += 4 * (int64_t)blockDim.x) {
             int32_t v[4];
@@ -113,6 +204,7 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
         offsets[e] = scan[e];
         if (tile_offsets) tile_offsets[e] = tscan[e];
     }
+    if (table != nullptr) build_tile_table(scan, E, bm, table);
     // cnt[w][e] becomes warp w's first position for expert e
     for (int e = tid; e < E; e += blockDim.x) {
         int32_t pos = scan[e];
@@ -149,15 +241,18 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
 
 cudaError_t launch_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                              int32_t* counts, int32_t* offsets, int32_t* perm,
-                             int32_t* tile_offsets, int bm, float* y, int64_t N,
+                             int32_t* tile_offsets, int bm, int4* tile_table, float* y, int64_t N,
                              int32_t* d_err, cudaStream_t s) {
     if (E > kMaxExperts) return cudaErrorInvalidValue;
     const int64_t P = T * topk;
-    const int smem = (int)((kRouteWarps * E + 2 * (E + 1) + (P <= kStageMax ? P : 0)) * 4);
+    const int64_t base = (kRouteWarps * (int64_t)E + 2 * (E + 1)) * 4;
+    const bool staged = base + P * 4 <= kStageBytes;
+    const int smem = (int)(base + (staged ? P * 4 : 0));
     cudaError_t e = ensure_smem_attr((const void*)moe_route_kernel, smem, 8);
     if (e != cudaSuccess) return e;
     return launch_pdl(moe_route_kernel, dim3(1), dim3(kRouteWarps * 32), (size_t)smem, s, topk_ids, P,
-                      E, counts, offsets, perm, tile_offsets, bm < 1 ? 1 : bm, y, N, d_err);
+                      E, counts, offsets, perm, tile_offsets, bm < 1 ? 1 : bm, tile_table, y, N, d_err,
+                      staged);
 }
 
 }  // namespace qg
