@@ -18,7 +18,9 @@
 //   pre-pass    activation codes widened to binary16 once per call (for the
 //               MoE product also gathered into expert order with their
 //               scales); dense: the weight codes widened to binary16 too and
-//               the weight scales transposed to group-major binary32.
+//               the weight scales transposed to group-major binary32, all
+//               three in one launch.  Each kernel of a call is a programmatic
+//               dependent launch of the one before.
 //   warp 16     TMA producer: binary16 A stages (one pair of groups, 128-byte
 //               swizzle, the operand layout the MMA reads directly); dense:
 //               a binary16 B stage of the same form on the same barrier, and
