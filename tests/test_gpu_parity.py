@@ -516,6 +516,63 @@ def test_grouped_moe_small(mode, K):
     assert_close(to_np(y), y_ref, mag)
 
 
+def _replay_in_graph(call):
+    """Capture call() in a CUDA graph (after one eager run on a side stream, which
+    capture needs) and replay it twice."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    return g
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_tc_dense_call_replays_in_cuda_graph(bits):
+    """A tensor-core product is a chain of programmatic dependent launches (pre-pass,
+    GEMM, tail reduction); captured in a CUDA graph the chain becomes graph edges, and
+    every replay gives the eager result bit for bit."""
+    M, N, K = 300, 520, 1024
+    qx, dx, qw, dw = _case(M, N, K, bits, 9090 + bits)
+    args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    y_eager = _gemm(bits, qg.ALGO_TCGEN05, *args)
+    _sync()
+    y = torch.empty_like(y_eager)
+    g = _replay_in_graph(lambda: _gemm(bits, qg.ALGO_TCGEN05, *args, y=y))
+    for _ in range(2):
+        y.fill_(float("nan"))
+        g.replay()
+        _sync()
+        assert torch.equal(y, y_eager)
+    assert qg.device_error() == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_grouped_moe_replays_in_cuda_graph(mode):
+    """The grouped product (routing with its tile table, gather, tensor-core GEMM) in a
+    CUDA graph: every replay gives the eager result bit for bit."""
+    rng, qw4, dw, ids = _moe_small(K=512)
+    T, topk = ids.shape
+    rows = T if mode == 0 else T * topk
+    qx, dx = oracle.quantize_act_q8(rng.standard_normal((rows, 512)).astype(np.float32))
+    a = (to_dev(qx), to_dev(dx), to_dev(ids), mode, to_dev(qw4), to_dev(dw))
+    y_eager, _ = qg.grouped_qgemm_moe(*a)
+    _sync()
+    y = torch.empty_like(y_eager)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    g = _replay_in_graph(lambda: qg.grouped_qgemm_moe(*a, y=y, d_err=err))
+    for _ in range(2):
+        y.fill_(float("nan"))
+        g.replay()
+        _sync()
+        assert torch.equal(y, y_eager)
+    assert int(to_np(err)[0]) == 0 and qg.device_error() == 0
+
+
 @pytest.mark.parametrize("K", [128, 256])
 def test_grouped_moe_unrouted_rows_zero_and_counted(K):
     rng, qw4, dw, ids = _moe_small(K=K)
