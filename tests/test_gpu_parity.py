@@ -346,10 +346,12 @@ def test_decode_step_as_benchmarked(M):
 # ------------------------------------------------------------------ GEMV with the quantization fused
 
 # (M, N, K, x row padding): K-splits W = 1, 2, 4 and 8 among them, a ragged last row
-# tile, and rows padded by 3 floats (not 16-byte aligned: scalar x loads)
+# tile, and rows padded by 3 floats (not 16-byte aligned: scalar x loads); from 8192
+# rows at M >= 2 the activations are staged per block (row tiles ragged at N = 8203 and
+# 9001)
 FUSED_SHAPES = [(1, 4096, 4096, 0), (4, 4096, 4096, 0), (1, 300, 12288, 0), (3, 37, 96, 3),
                 (8, 1000, 1024, 0), (2, 33, 12288, 3), (7, 129, 4160, 0), (1, 5, 32, 0),
-                (5, 40000, 512, 0)]
+                (5, 40000, 512, 0), (8, 8203, 1024, 3), (2, 9001, 256, 0), (4, 12288, 4096, 0)]
 
 
 @pytest.mark.parametrize("M,N,K,pad", FUSED_SHAPES)
