@@ -575,6 +575,32 @@ def test_grouped_moe_replays_in_cuda_graph(mode):
     assert int(to_np(err)[0]) == 0 and qg.device_error() == 0
 
 
+def test_tc_chains_on_a_side_stream():
+    """The programmatic dependent launches of a call stay on the caller's stream: the
+    tensor-core dense and grouped products issued on a side stream, right after work
+    that writes their inputs on that stream, equal the default-stream results."""
+    M, N, K = 200, 384, 1024
+    qx, dx, qw, dw = _case(M, N, K, 8, 4711)
+    args = (to_dev(qx), to_dev(dx), to_dev(qw), to_dev(dw))
+    y_ref = _gemm(8, qg.ALGO_TCGEN05, *args)
+    rng, qw4, dw4, ids = _moe_small(K=512)
+    qx2, dx2 = oracle.quantize_act_q8(rng.standard_normal((ids.shape[0], 512)).astype(np.float32))
+    a = (to_dev(qx2), to_dev(dx2), to_dev(ids), 0, to_dev(qw4), to_dev(dw4))
+    ym_ref, _ = qg.grouped_qgemm_moe(*a)
+    _sync()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        qx_s = torch.empty_like(args[0])
+        qx_s.copy_(args[0])                          # the input is written on the side stream
+        y = _gemm(8, qg.ALGO_TCGEN05, qx_s, *args[1:])
+        ym, err = qg.grouped_qgemm_moe(*a)
+    torch.cuda.current_stream().wait_stream(side)
+    _sync()
+    assert torch.equal(y, y_ref) and torch.equal(ym, ym_ref)
+    assert int(to_np(err)[0]) == 0 and qg.device_error() == 0
+
+
 @pytest.mark.parametrize("K", [128, 256])
 def test_grouped_moe_unrouted_rows_zero_and_counted(K):
     rng, qw4, dw, ids = _moe_small(K=K)
