@@ -14,9 +14,10 @@
 // (optional), counting them in *d_err without trapping.
 //
 // Stability without a global sort: warp w owns the contiguous slice w of the
-// pairs (read from a shared-memory copy of the ids when they fit).  Phase 1 counts experts per warp; phase 2 turns the per-warp counts
-// into starting positions (expert-major, then warp order); phase 3 walks each
-// slice in order 32 pairs at a time, ranks equal experts inside the step with
+// pairs (read from a shared-memory copy of the ids when they fit).  Phase 1
+// counts experts per warp; phase 2 turns the per-warp counts into starting
+// positions (expert-major, then warp order); phase 3 walks each slice in order
+// 32 pairs at a time, ranks equal experts inside the step with
 // __match_any_sync, and advances the warp's private cursor of each expert.
 #include "common.cuh"
 #include "kernels.h"
