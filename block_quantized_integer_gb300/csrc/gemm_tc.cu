@@ -1205,7 +1205,6 @@ cudaError_t launch_tc_grouped(const int8_t* qx, const float* dx, int64_t P, int6
                               int32_t topk, int32_t x_row_mode, const int32_t* perm,
                               const int32_t* offsets, const int32_t* tile_offsets,
                               void* workspace, cudaStream_t s) {
-    const int64_t G = K / kGroup;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* a16 = reinterpret_cast<__half*>(ws);
     float* dxg = reinterpret_cast<float*>(ws + align16((size_t)P * K * 2));
